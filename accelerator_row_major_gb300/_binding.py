@@ -1,0 +1,130 @@
+"""ctypes binding of libgemm_f32.so: argument marshalling only.
+
+Every computation happens in the library's CUDA kernels.  The library is
+loaded on first use; if it is missing, that first call raises ImportError.
+There is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgemm_f32.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "gemm_f32.h")
+
+GEMM_F32_OK = 0
+GEMM_F32_EINVAL = -1
+GEMM_F32_EDEVICE = -2
+GEMM_F32_ELAUNCH = -3
+GEMM_F32_ETIMEOUT = -4
+
+MODE_TC3X = 0
+MODE_FFMA = 1
+MODE_TC1X = 2
+MODES = {"tc3x": MODE_TC3X, "ffma": MODE_FFMA, "tc1x": MODE_TC1X}
+
+FLAG_FORCE_STAGED = 0x1
+FLAG_TILE64 = 0x10
+FLAG_TILE128 = 0x20
+FLAG_TILE256 = 0x40
+FLAG_ONE_TILE_PER_CTA = 0x100
+
+_ERRORS = {
+    GEMM_F32_EINVAL: "invalid argument",
+    GEMM_F32_EDEVICE: "unsupported device (needs sm_103, GB300)",
+    GEMM_F32_ELAUNCH: "kernel launch refused by the CUDA runtime",
+    GEMM_F32_ETIMEOUT: "a bounded device-side wait ran out",
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s failed: %s (%d)" % (what, _ERRORS.get(code, "unknown error"), code))
+        self.code = code
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError("libgemm_f32.so is not built (run accelerator_row_major_gb300.build.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, cu = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
+    lib.gemm_f32.argtypes = [vp, vp, vp, ci, ci, ci, vp]
+    lib.gemm_f32.restype = ci
+    lib.gemm_f32_ex.argtypes = [vp, vp, vp, ci, ci, ci, ci, cu, vp]
+    lib.gemm_f32_ex.restype = ci
+    lib.gemm_f32_status.argtypes = [vp, ctypes.POINTER(cu)]
+    lib.gemm_f32_status.restype = ci
+    lib.gemm_f32_last_launches.argtypes = []
+    lib.gemm_f32_last_launches.restype = ci
+    lib.gemm_f32_version.argtypes = []
+    lib.gemm_f32_version.restype = ctypes.c_char_p
+    return lib
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (loaded once, on first use)."""
+    global _lib
+    if _lib is None:
+        _lib = _load()
+    return _lib
+
+
+def declared_symbols(header: str = HEADER):
+    """Function names declared in include/gemm_f32.h."""
+    with open(header) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f32\w*)\s*\(", text)))
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(s) -> int:
+    if s is None:
+        return 0
+    if isinstance(s, int):
+        return s
+    return int(s.cuda_stream)
+
+
+def gemm_f32(A, B, C, M: int, N: int, K: int, stream=None) -> int:
+    """C = A * B (row-major, default mode).  A, B, C: device pointers (int)
+    or CUDA tensors; stream: int handle, torch.cuda.Stream or None."""
+    return lib().gemm_f32(_ptr(A), _ptr(B), _ptr(C), M, N, K, _stream(stream))
+
+
+def gemm_f32_ex(A, B, C, M: int, N: int, K: int, mode=MODE_TC3X, flags: int = 0, stream=None) -> int:
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return lib().gemm_f32_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(mode), int(flags), _stream(stream))
+
+
+def gemm_f32_status(stream=None):
+    """(code, site): synchronises the stream, reads and clears the error word."""
+    site = ctypes.c_uint(0)
+    rc = lib().gemm_f32_status(_stream(stream), ctypes.byref(site))
+    return rc, site.value
+
+
+def gemm_f32_last_launches() -> int:
+    return lib().gemm_f32_last_launches()
+
+
+def gemm_f32_version() -> str:
+    return lib().gemm_f32_version().decode()
+
+
+def check(rc: int, what: str = "gemm_f32") -> None:
+    if rc != GEMM_F32_OK:
+        raise GemmError(rc, what)

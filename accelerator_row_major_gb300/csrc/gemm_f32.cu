@@ -1,0 +1,174 @@
+// C-ABI front end of libgemm_f32: argument checks, per-device set-up, the
+// K == 0 case, mode selection and the device error word.  The operation and
+// the contract of each entry point are documented in include/gemm_f32.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_f32.h"
+#include "launch.h"
+
+namespace {
+
+// One error word per device: 0, or the site code of the first bounded wait
+// that ran out since the last gemm_f32_status() on that device.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int status = GEMM_F32_EDEVICE;  // GEMM_F32_OK once set up
+  int num_sms = 0;
+  unsigned* err = nullptr;        // device address of g_error_word
+};
+
+DeviceState g_devices[kMaxDevices];
+thread_local int t_last_launches = 0;
+
+// Set-up runs once per device, with that device current: checks it is an
+// sm_103 part, reads the SM count, takes the address of the error word and
+// clears it.
+DeviceState* device_state(int* device_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  *device_out = dev;
+  DeviceState& st = g_devices[dev];
+  std::call_once(st.once, [&st, dev] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return;
+    }
+    if (major != 10 || minor != 3) return;  // the kernels are built for sm_103a only
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return;
+    }
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return;
+    }
+    st.num_sms = sms;
+    st.err = static_cast<unsigned*>(p);
+    st.status = GEMM_F32_OK;
+  });
+  return &st;
+}
+
+int default_mode() {
+  static const int mode = [] {
+    const char* s = std::getenv("GEMM_F32_MODE");
+    if (s && std::strcmp(s, "ffma") == 0) return static_cast<int>(GEMM_F32_MODE_FFMA);
+    if (s && std::strcmp(s, "tc1x") == 0) return static_cast<int>(GEMM_F32_MODE_TC1X);
+    return static_cast<int>(GEMM_F32_MODE_TC3X);
+  }();
+  return mode;
+}
+
+bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a_bytes && b_bytes && a0 < b0 + b_bytes && b0 < a0 + a_bytes;
+}
+
+constexpr unsigned kKnownFlags = GEMM_F32_FLAG_FORCE_STAGED | GEMM_F32_FLAG_TILE64 |
+                                 GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
+                                 GEMM_F32_FLAG_ONE_TILE_PER_CTA;
+
+}  // namespace
+
+extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
+                           unsigned flags, gemm_f32_stream_t stream_handle) {
+  t_last_launches = 0;
+  // ---- host-only checks first: no CUDA call for a malformed request
+  if (M < 0 || N < 0 || K < 0) return GEMM_F32_EINVAL;
+  if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_FFMA && mode != GEMM_F32_MODE_TC1X)
+    return GEMM_F32_EINVAL;
+  if (flags & ~kKnownFlags) return GEMM_F32_EINVAL;
+  const unsigned bn_flags = flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256);
+  if (bn_flags & (bn_flags - 1)) return GEMM_F32_EINVAL;  // at most one tile width
+  if (M == 0 || N == 0) return GEMM_F32_OK;
+  const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+  const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * sizeof(float);
+  const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * sizeof(float);
+  if (C == nullptr) return GEMM_F32_EINVAL;
+  if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_F32_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 3u)
+    return GEMM_F32_EINVAL;
+  if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return GEMM_F32_EINVAL;
+
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+
+  if (K == 0) {  // an empty sum: C = 0
+    if (cudaMemsetAsync(C, 0, c_bytes, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
+    t_last_launches = 1;
+    return GEMM_F32_OK;
+  }
+
+  gemm_f32_impl::GemmArgs g;
+  g.A = A;
+  g.B = B;
+  g.C = C;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.err = st->err;
+  g.num_sms = st->num_sms;
+  g.device = dev;
+  g.flags = flags;
+  int launches = 0;
+  int rc;
+  if (mode == GEMM_F32_MODE_FFMA)
+    rc = gemm_f32_impl::launch_ffma(g, stream, &launches);
+  else
+    rc = gemm_f32_impl::launch_tc(g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream, &launches);
+  if (rc == GEMM_F32_OK) t_last_launches = launches;
+  return rc;
+}
+
+extern "C" int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K,
+                        gemm_f32_stream_t stream) {
+  return gemm_f32_ex(A, B, C, M, N, K, default_mode(), 0u, stream);
+}
+
+extern "C" int gemm_f32_status(gemm_f32_stream_t stream_handle, unsigned* site) {
+  if (site) *site = 0;
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_handle)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
+  unsigned word = 0;
+  const unsigned zero = 0;
+  if (cudaMemcpy(&word, st->err, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(st->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
+  if (site) *site = word;
+  return word ? GEMM_F32_ETIMEOUT : GEMM_F32_OK;
+}
+
+extern "C" int gemm_f32_last_launches(void) { return t_last_launches; }
+
+extern "C" const char* gemm_f32_version(void) { return "gemm_f32 1.0 sm_103a"; }

@@ -1,0 +1,28 @@
+// Private interface between the C-ABI front end (gemm_f32.cu) and the
+// kernel translation units.  Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace gemm_f32_impl {
+
+struct GemmArgs {
+  const float* A;
+  const float* B;
+  float* C;
+  int M, N, K;          // K >= 1, M >= 1, N >= 1 here (the front end handles the rest)
+  unsigned* err;        // device error word of the current device
+  int num_sms;          // multiprocessors of the current device
+  int device;           // current device ordinal
+  unsigned flags;       // GEMM_F32_FLAG_* bits
+};
+
+// Tensor-core path (tcgen05.mma kind::tf32).  nprod = 3 (split hi/lo, three
+// products) or 1 (operands rounded to TF32, one product).  Returns 0 or a
+// negative GEMM_F32_E* code.  *launches receives the kernels launched.
+int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
+
+// CUDA-core FFMA path.
+int launch_ffma(const GemmArgs& g, cudaStream_t stream, int* launches);
+
+}  // namespace gemm_f32_impl

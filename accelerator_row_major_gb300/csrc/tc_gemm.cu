@@ -1,0 +1,515 @@
+// Tensor-core FP32 GEMM for sm_103a: tcgen05.mma kind::tf32 with a TMEM
+// accumulator, fed by TMA (or by masked per-thread loads where TMA cannot
+// address the operands), with the 3xTF32 split done in shared memory.
+//
+// Computes C[i][j] = sum_k A[i][k] * B[k][j] for row-major A (M x K),
+// B (K x N), C (M x N): the product of "LeetGPU problem 2: matrix
+// multiplication" (yekq.top, section "problem statement").  The pages tile
+// the product in shared memory with two barriers per K phase ("Lesson 10:
+// shared-memory tiled GEMM", hpc.payai.win, section 2); here the K phases
+// flow through a ring of stages guarded by mbarriers instead, and ragged
+// edges are zero-filled on load and masked on store as in the pages'
+// guarded tiles (same lesson, section 3; "LeetGPU problem 2", v3 tail fix).
+//
+// Tile: 128 columns of C (n) by TM rows (m).  Row-major B is N-contiguous,
+// and a kind::tf32 MMA only accepts K-major operands, so B is transposed on
+// its way into the tensor core: the transform warps read the raw B tile
+// (thread t owns column n0 + t) and write its TF32 hi/lo parts into tensor
+// memory, where lane t holds column t and one 32-bit column holds one k.
+// That is the MMA's A operand (M = 128 lanes); the A tile, K-major as it
+// sits in memory, is the MMA's shared-memory B operand (N = TM).  The MMA
+// therefore accumulates the transposed tile, D[n][m] = C[m][n], which also
+// makes the epilogue's stores coalesced (lane t writes column n0 + t).
+//
+// Roles inside one persistent CTA (one CTA per SM, 12 warps):
+//   warp 0        TMA producer: A tile [TM x BK] (swizzled) and B tile
+//                 [BK x 128] per K phase into stage s
+//   warp 1        TMEM allocator and MMA issuer (one thread)
+//   warps 4..7    epilogue: TMEM -> registers -> C (masked, coalesced)
+//   warps 8..11   transform: A tile -> TF32 hi (in place) and lo in shared
+//                 memory; B tile -> TF32 hi/lo of its transpose in TMEM.
+//                 On the staged path (operands TMA cannot address) these
+//                 warps load both tiles from global memory themselves.
+// Every role walks the same tile sequence and the same K-phase count, so
+// no role leaves a barrier phase unfinished (the uniform-control rule of
+// "Lesson 10", section 3).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_f32.h"
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace gemm_f32_impl {
+using namespace gemm_f32_dev;
+
+namespace {
+
+constexpr int kTN = 128;                     // columns of C per tile = TMEM lanes = MMA M
+constexpr int kWarps = 12;                   // see role table above
+constexpr int kThreads = kWarps * 32;
+constexpr int kEpilogueWarp0 = 4;
+constexpr int kTransformWarp0 = 8;
+constexpr int kTransformThreads = 128;
+constexpr int kEpilogueThreads = 128;
+constexpr int kSmemLimit = 232448;           // opt-in dynamic shared memory per block
+constexpr int kTmemCols = 512;
+constexpr int kRasterGroup = 8;              // tile-rows per L2 group
+
+struct TcParams {
+  const float* A;
+  const float* B;
+  float* C;
+  int M, N, K;
+  int tiles_m, tiles_n, k_iters;
+  unsigned* err;
+};
+
+template <int TM, int BK, int NPROD>
+struct TcCfg {
+  static constexpr int A_BYTES = TM * BK * 4;                       // A hi (TMA target)
+  static constexpr int A_LO_BYTES = NPROD == 3 ? A_BYTES : 0;       // A lo
+  static constexpr int B_RAW_BYTES = BK * kTN * 4;                  // raw B tile [BK][128]
+  static constexpr int STAGE_BYTES = A_BYTES + A_LO_BYTES + B_RAW_BYTES;
+  static constexpr int NACC = TM == 256 ? 1 : 2;                    // accumulators in TMEM
+  static constexpr int ACC_COLS = NACC * TM;
+  static constexpr int BT_COLS = BK * (NPROD == 3 ? 2 : 1);         // B^T hi (+ lo) per stage
+  static constexpr int FIT_SMEM = (kSmemLimit - 2048) / STAGE_BYTES;
+  static constexpr int FIT_TMEM = (kTmemCols - ACC_COLS) / BT_COLS;
+  static constexpr int S0 = FIT_SMEM < FIT_TMEM ? FIT_SMEM : FIT_TMEM;
+  static constexpr int STAGES = S0 < 8 ? S0 : 8;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 1024;
+  static constexpr uint32_t A_SWZ_MASK = BK == 32 ? 7u : 3u;       // 128B or 64B swizzle
+  static constexpr uint32_t A_LAYOUT = BK == 32 ? 2u : 4u;         // descriptor layout code
+  static constexpr uint32_t A_SBO = BK == 32 ? 1024u : 512u;       // 8-row group stride
+  static_assert(STAGES >= 2, "at least two stages");
+  static_assert(BK == 16 || BK == 32, "BK");
+  static_assert(TM == 64 || TM == 128 || TM == 256, "TM");
+  static_assert(A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "1024-byte aligned atoms");
+  static_assert(ACC_COLS + STAGES * BT_COLS <= kTmemCols, "TMEM budget");
+};
+
+// Byte offset of a swizzled tile element from its plain (row-major in the
+// tile) offset: the 16-byte chunk index is XORed with bits 7.. of the offset,
+// which is how TMA writes and tcgen05 reads 64B / 128B swizzled tiles.
+__device__ __forceinline__ uint32_t swizzle(uint32_t o, uint32_t mask) {
+  return o ^ (((o >> 7) & mask) << 4);
+}
+
+template <int BK>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t (&v)[BK]);
+template <>
+__device__ __forceinline__ void tmem_store_cols<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+  tmem_st_16cols(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_store_cols<32>(uint32_t taddr, const uint32_t (&v)[32]) {
+  tmem_st_32cols(taddr, v);
+}
+
+template <int TM, int BK, int NPROD, bool TMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  using Cfg = TcCfg<TM, BK, NPROD>;
+  constexpr int S = Cfg::STAGES;
+  constexpr int NACC = Cfg::NACC;
+  extern __shared__ uint8_t smem_dyn[];
+  const uint32_t dyn0 = smem_addr(smem_dyn);
+  const uint32_t base = (dyn0 + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_dyn + (base - dyn0);
+  const uint32_t bars = base + S * Cfg::STAGE_BYTES;
+  // barrier map (8 bytes each)
+  auto full_bar = [&](int s) { return bars + 8u * s; };              // TMA landed
+  auto ready_bar = [&](int s) { return bars + 8u * (S + s); };       // operands split
+  auto empty_bar = [&](int s) { return bars + 8u * (2 * S + s); };   // MMAs done with stage
+  auto accf_bar = [&](int b) { return bars + 8u * (3 * S + b); };    // accumulator b complete
+  auto acce_bar = [&](int b) { return bars + 8u * (3 * S + NACC + b); };  // accumulator b drained
+  const uint32_t drain_bar = bars + 8u * (3 * S + 2 * NACC);
+  const uint32_t tmem_slot = drain_bar + 8u;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(ready_bar(s), kTransformThreads);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < NACC; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), kEpilogueThreads);
+    }
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (TMA && warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+
+  const int num_tiles = p.tiles_m * p.tiles_n;
+  const int k_iters = p.k_iters;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
+    if (TMA && lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t armed = 0;    // bit s: stage s was armed at least once
+      uint32_t last_ph = 0;  // bit s: parity of the last arming of stage s
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
+        for (int kt = 0; kt < k_iters; ++kt) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = base + s * Cfg::STAGE_BYTES;
+          mbar_arrive_expect_tx(full_bar(s), Cfg::A_BYTES + Cfg::B_RAW_BYTES);
+          armed |= 1u << s;
+          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+          tma_load_2d(st, &tmA, full_bar(s), kt * BK, c.tm * TM);
+          tma_load_2d(st + Cfg::A_BYTES + Cfg::A_LO_BYTES, &tmB, full_bar(s), c.tn * kTN, kt * BK);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // copies still in flight must land before the CTA's shared memory goes away
+      for (int q = 0; q < S; ++q)
+        if (armed & (1u << q)) mbar_wait(full_bar(q), (last_ph >> q) & 1u, p.err, kSiteDrainTma);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(kTN, TM, false, false);
+      int s = 0;
+      uint32_t ph = 0;
+      int acc = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+        if (!mbar_wait(acce_bar(acc), acc_ph ^ 1u, p.err, kSiteMmaAccEmpty)) break;
+        tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TM);
+        for (int kt = 0; kt < k_iters; ++kt) {
+          if (!mbar_wait(ready_bar(s), ph, p.err, kSiteMmaReady)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t st = base + s * Cfg::STAGE_BYTES;
+          const uint32_t bt = tmem_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS);
+#pragma unroll
+          for (int kk = 0; kk < BK / 8; ++kk) {
+            const uint64_t a_hi = smem_desc(st + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
+            mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_hi, idesc, (kt | kk) != 0 ? 1u : 0u);
+            if (NPROD == 3) {
+              const uint64_t a_lo =
+                  smem_desc(st + Cfg::A_BYTES + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
+              mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_lo, idesc, 1u);        // B_hi * A_lo
+              mma_tf32_tmem_a(d_tmem, bt + BK + kk * 8, a_hi, idesc, 1u);   // B_lo * A_hi
+            }
+          }
+          mma_commit(empty_bar(s));  // stage s is free once these MMAs finish
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(accf_bar(acc));   // accumulator complete once all MMAs finish
+        if (++acc == NACC) {
+          acc = 0;
+          acc_ph ^= 1u;
+        }
+      }
+      mma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, p.err, kSiteDrainMma);
+    }
+    __syncwarp();
+  } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
+    int acc = 0;
+    uint32_t acc_ph = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
+      if (!mbar_wait(accf_bar(acc), acc_ph, p.err, kSiteEpilogueFull)) break;
+      tc_fence_after_sync();
+      const int n = c.tn * kTN + q * 32 + lane;     // this thread's column of C
+      const bool n_ok = n < p.N;
+#pragma unroll 1
+      for (int chunk = 0; chunk < TM / 32; ++chunk) {
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>(acc * TM + chunk * 32),
+                       v);
+        tmem_wait_ld();
+        const int m0 = c.tm * TM + chunk * 32;
+        if (n_ok) {
+          float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(p.N) + n;
+          const int rows = min(32, p.M - m0);
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < rows) dst[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(acce_bar(acc));
+      if (++acc == NACC) {
+        acc = 0;
+        acc_ph ^= 1u;
+      }
+    }
+  } else if (warp >= kTransformWarp0) {
+    // ------------------------------------------------------------ transform
+    const int tt = threadIdx.x - kTransformWarp0 * 32;   // = this thread's TMEM lane
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(tt & ~31) << 16);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
+      for (int kt = 0; kt < k_iters; ++kt) {
+        uint8_t* const st = base_ptr + s * Cfg::STAGE_BYTES;
+        // the MMAs of this stage's previous round must be done before its
+        // TMEM columns are overwritten (implied on the TMA path, cheap to check)
+        if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteTransformEmpty)) {
+          ok = false;
+          break;
+        }
+        if (TMA && !mbar_wait(full_bar(s), ph, p.err, kSiteTransformFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t bh[BK], bl[BK];
+        if (TMA) {
+          // A: split in place (layout preserving), lo to its own buffer
+          uint4* const hi = reinterpret_cast<uint4*>(st);
+          uint4* const lo = reinterpret_cast<uint4*>(st + Cfg::A_BYTES);
+#pragma unroll 4
+          for (int i = tt; i < Cfg::A_BYTES / 16; i += kTransformThreads) {
+            const uint4 x = hi[i];
+            uint4 h, l;
+            tf32_split(x.x, h.x, l.x);
+            tf32_split(x.y, h.y, l.y);
+            tf32_split(x.z, h.z, l.z);
+            tf32_split(x.w, h.w, l.w);
+            hi[i] = h;
+            if (NPROD == 3) lo[i] = l;
+          }
+          // B: column tt of the raw tile
+          const uint32_t* braw =
+              reinterpret_cast<const uint32_t*>(st + Cfg::A_BYTES + Cfg::A_LO_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK; ++k) tf32_split(braw[k * kTN + tt], bh[k], bl[k]);
+        } else {
+          const int m0 = c.tm * TM, n0 = c.tn * kTN, k0 = kt * BK;
+          // A tile: row r, column k; lanes run along k (coalesced)
+#pragma unroll 2
+          for (int e = tt; e < TM * BK; e += kTransformThreads) {
+            const int r = e / BK, k = e % BK;
+            const int gm = m0 + r, gk = k0 + k;
+            const uint32_t x = (gm < p.M && gk < p.K)
+                                   ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
+                                   : 0u;
+            uint32_t h, l;
+            tf32_split(x, h, l);
+            const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
+            *reinterpret_cast<uint32_t*>(st + o) = h;
+            if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+          }
+          // B tile: column n0 + tt, rows k0 .. k0+BK-1 (lanes along n: coalesced)
+          const int gn = n0 + tt;
+#pragma unroll
+          for (int k = 0; k < BK; ++k) {
+            const int gk = k0 + k;
+            const uint32_t x = (gn < p.N && gk < p.K)
+                                   ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
+                                   : 0u;
+            tf32_split(x, bh[k], bl[k]);
+          }
+        }
+        const uint32_t bt = lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS);
+        tmem_store_cols<BK>(bt, bh);
+        if (NPROD == 3) tmem_store_cols<BK>(bt + BK, bl);
+        tmem_wait_st();
+        fence_proxy_async_smem();  // A hi/lo: generic-proxy writes -> tensor-core reads
+        tc_fence_before_sync();
+        mbar_arrive(ready_bar(s));
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      (void)cudaGetLastError();
+  });
+  return g_encode;
+}
+
+// 2-D fp32 map of a row-major [rows x cols] matrix, box [box_rows x box_cols].
+bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_cols, int box_rows,
+               CUtensorMapSwizzle swz) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int TM, int BK, int NPROD, bool TMA>
+int launch_one(const GemmArgs& g, const TcParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
+               int grid, cudaStream_t stream) {
+  using Cfg = TcCfg<TM, BK, NPROD>;
+  static std::atomic<unsigned long long> configured{0};  // bit per device
+  auto kern = tc_gemm_kernel<TM, BK, NPROD, TMA>;
+  const unsigned long long bit = 1ull << (g.device % kMaxDevices);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
+    configured.fetch_or(bit);
+  }
+  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  return GEMM_F32_OK;
+}
+
+template <int BK, int NPROD, bool TMA>
+int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const CUtensorMap& ma,
+              const CUtensorMap& mb, int grid, cudaStream_t stream) {
+  switch (tm) {
+    case 64: return launch_one<64, BK, NPROD, TMA>(g, p, ma, mb, grid, stream);
+    case 128: return launch_one<128, BK, NPROD, TMA>(g, p, ma, mb, grid, stream);
+    default: return launch_one<256, BK, NPROD, TMA>(g, p, ma, mb, grid, stream);
+  }
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Tile height TM: the one whose persistent schedule gives the busiest SM the
+// least work (rounds x TM, plus a per-tile overhead), preferring taller tiles
+// on a tie (each B panel is then split fewer times).
+int choose_tm(const GemmArgs& g) {
+  if (g.flags & GEMM_F32_FLAG_TILE64) return 64;
+  if (g.flags & GEMM_F32_FLAG_TILE128) return 128;
+  if (g.flags & GEMM_F32_FLAG_TILE256) return 256;
+  const long tn = ceil_div(g.N, kTN);
+  long best_cost = -1;
+  int best = 256;
+  for (int tm : {256, 128, 64}) {
+    const long tiles = tn * ceil_div(g.M, tm);
+    const long rounds = (tiles + g.num_sms - 1) / g.num_sms;
+    const long cost = rounds * (tm + 16);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = tm;
+    }
+  }
+  return best;
+}
+
+}  // namespace
+
+int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+  *launches = 0;
+  const int tm = choose_tm(g);
+  const int bk = nprod == 3 ? 16 : 32;
+  TcParams p;
+  p.A = g.A;
+  p.B = g.B;
+  p.C = g.C;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles_m = ceil_div(g.M, tm);
+  p.tiles_n = ceil_div(g.N, kTN);
+  p.k_iters = ceil_div(g.K, bk);
+  p.err = g.err;
+  const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
+  const int grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
+                       ? static_cast<int>(tiles)
+                       : static_cast<int>(std::min<long>(tiles, g.num_sms));
+
+  // TMA needs 16-byte aligned bases and row strides (K % 4 == 0, N % 4 == 0).
+  bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && g.K % 4 == 0 && g.N % 4 == 0 &&
+             reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+  alignas(64) CUtensorMap ma, mb;
+  if (tma) {
+    tma = encode_2d(&ma, g.A, g.M, g.K, bk, tm,
+                    bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
+          encode_2d(&mb, g.B, g.K, g.N, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!tma) {
+    memset(&ma, 0, sizeof(ma));
+    memset(&mb, 0, sizeof(mb));
+  }
+  int rc;
+  if (nprod == 3) {
+    rc = tma ? launch_tm<16, 3, true>(tm, g, p, ma, mb, grid, stream)
+             : launch_tm<16, 3, false>(tm, g, p, ma, mb, grid, stream);
+  } else {
+    rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
+             : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
+  }
+  if (rc == GEMM_F32_OK) *launches = 1;
+  return rc;
+}
+
+}  // namespace gemm_f32_impl

@@ -1,0 +1,408 @@
+#!/usr/bin/env python3
+"""Throughput of the row-major FP32 GEMM on GB300; prints ONE JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5a]
+                    [--mode tc3x|ffma|tc1x] [--impl ours|reference]
+
+A step is one product C = A * B of the named problem (workloads.py) through
+the C ABI (one kernel launch).  Inputs are synthetic, seeded, resident in
+device memory when the timed region starts; K steps are timed with CUDA
+events on the launching stream, bracketed by a barrier and a synchronise.
+Problems whose operands fit twice in L2 get an L2 flush between steps
+(each step timed on its own); the default 8192^3 problem's operands are
+larger than L2.  `value` is whole-job TFLOPS = 2MNK * ranks / max-over-ranks
+time.  The e2e figure times the same call with host buffers: pinned host ->
+device copies of A and B, the product, and the device -> host copy of C.
+
+With N > 1 (torchrun) every rank runs its own replica of the problem on its
+own GPU: the product needs no exchange between GPUs, so scaling is weak.
+
+--impl reference times the CPU oracle (the only other implementation of the
+same computation here) on a bounded sample of the same problem: the first R
+rows of A times all of B, R chosen so the run ends within a few minutes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "FP32 GEMM TFLOPS (2MNK/t) at 1 GB300 and % of 3xTF32 / FFMA roofline"
+L2_BYTES = 129 * 1024 * 1024
+# nominal dense ratios (tf32 : bf16 tensor rate) used to scale the measured bf16 peak
+TF32_PER_BF16 = 1.1 / 2.25
+# CUDA-core fp32: 128 lanes x 2 FLOP per SM per clock
+FFMA_FLOP_PER_SM_CLK = 256
+MODE_PRODUCTS = {"tc3x": 3, "tc1x": 1, "ffma": 1}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c5a", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--mode", default="tc3x", choices=sorted(MODE_PRODUCTS))
+    ap.add_argument("--flags", type=lambda s: int(s, 0), default=0, help="gemm_f32_ex flags (tuning)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed plumbing
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+    return dist
+
+
+def barrier(dist_mod, device=None):
+    if dist_mod is not None:
+        if device is not None and device.type == "cuda":
+            dist_mod.barrier(device_ids=[device.index])
+        else:
+            dist_mod.barrier()
+
+
+def max_over_ranks(value: float, dist_mod, device) -> float:
+    """Largest value over all ranks (the job ends when its slowest rank does)."""
+    if dist_mod is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist_mod.all_reduce(t, op=dist_mod.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_step: int, steps: int, world: int, max_seconds: float) -> float:
+    """Aggregate throughput: every rank did `steps` products; the job took the max time."""
+    return flop_per_step * steps * world / max_seconds / 1e12
+
+
+# ---------------------------------------------------------------- peaks, clocks, traffic
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while active."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, enabled: bool = True):
+        self.index = index
+        self.proc = None
+        self.enabled = enabled
+
+    def __enter__(self):
+        if self.enabled:
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                     "--format=csv,noheader,nounits", "-lms", "100"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        rows = []
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, v in enumerate(flags) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "accelerator_row_major_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, config: str, mode: str):
+    """DRAM bytes per launch from a committed ncu capture of the same sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    rec = table.get("%s/%s/%s" % (kernel, config, mode))
+    if not rec or rec.get("source_sha") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample(A, B, seconds: float):
+    """Time the oracle on the first R rows of A; R grows until ~`seconds`."""
+    import oracle
+    M, K = A.shape
+    N = B.shape[1]
+    rows = 1
+    while True:
+        t0 = time.perf_counter()
+        oracle.gemm(A[:rows], B)
+        dt = time.perf_counter() - t0
+        if dt >= seconds / 8 or rows >= M:
+            break
+        rows = min(M, rows * 4)
+    rows = max(1, min(M, int(rows * seconds / max(dt, 1e-6))))
+    t0 = time.perf_counter()
+    oracle.gemm(A[:rows], B)
+    dt = time.perf_counter() - t0
+    tflops = workloads.gemm_flops(rows, N, K) / dt / 1e12
+    return {"value": tflops, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": "first %d of %d rows of A times all of B (%dx%dx%d), fp64 accumulation plus "
+                      "|A||B|, %.1f s" % (rows, M, rows, K, N, dt)}, rows
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    p = workloads.CONFIGS[args.config]
+    A, B = workloads.make_inputs(p.M, p.K, p.N, p.law, p.seed)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    _, rows = oracle_sample(A, B, min(budget, 5.0))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(A[:rows], B)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    t = sum(times) / len(times)
+    value = workloads.gemm_flops(rows, p.N, p.K) / t / 1e12
+    sample = "first %d of %d rows of A times all of B per step (%dx%dx%d)" % (rows, p.M, rows, p.K, p.N)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": "%s: %dx%dx%d (M,K,N) fp32 row-major, %s, seed %d" %
+                       (p.name, p.M, p.K, p.N, p.law, p.seed), "sample_rows": rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.max_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU timing
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local_rank = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    dist_mod = init_dist(world, "nccl")
+
+    from accelerator_row_major_gb300 import build as build_mod
+    build_mod.build()
+    import accelerator_row_major_gb300 as g
+
+    p = workloads.CONFIGS[args.config]
+    M, K, N = p.M, p.K, p.N
+    A_h, B_h = workloads.make_inputs(M, K, N, p.law, p.seed)
+    stream = torch.cuda.Stream(device)
+    A = torch.from_numpy(A_h).to(device)
+    B = torch.from_numpy(B_h).to(device)
+    C = torch.empty((M, N), dtype=torch.float32, device=device)
+    flop = workloads.gemm_flops(M, N, K)
+    work_bytes = workloads.algorithmic_bytes(M, N, K)
+    flush = work_bytes < 2 * L2_BYTES
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) if flush else None
+
+    def step():
+        rc = g.gemm_f32_ex(A, B, C, M, N, K, args.mode, args.flags, stream)
+        if rc != 0:
+            raise g.GemmError(rc, "gemm_f32_ex")
+
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step()
+    launches_per_step = g.gemm_f32_last_launches()
+    rc, site = g.gemm_f32_status(stream)
+    if rc != 0:
+        raise SystemExit("device error word %d after warm-up" % site)
+
+    events = []
+    with ClockSampler(local_rank, enabled=not args.no_clocks) as clocks:
+        barrier(dist_mod, device)
+        torch.cuda.synchronize(device)
+        with torch.cuda.stream(stream):
+            if flush:
+                for _ in range(args.steps):
+                    scratch.zero_()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    step()
+                    e1.record(stream)
+                    events.append((e0, e1))
+            else:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(args.steps):
+                    step()
+                e1.record(stream)
+                events.append((e0, e1))
+        torch.cuda.synchronize(device)
+        barrier(dist_mod, device)
+    device_ms = sum(a.elapsed_time(b) for a, b in events)
+    rc, site = g.gemm_f32_status(stream)
+    if rc != 0:
+        raise SystemExit("device error word %d in the timed region" % site)
+    ms_per_step = max_over_ranks(device_ms / args.steps, dist_mod, device)
+    value = whole_job_tflops(flop, args.steps, world, ms_per_step * args.steps / 1e3)
+
+    # ---- end to end through the public call with host buffers
+    e2e = None
+    if not args.no_e2e:
+        A_pin = torch.from_numpy(A_h).pin_memory()
+        B_pin = torch.from_numpy(B_h).pin_memory()
+        C_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
+        e2e_steps = max(3, args.steps // 4)
+
+        def e2e_step():
+            A.copy_(A_pin, non_blocking=True)
+            B.copy_(B_pin, non_blocking=True)
+            step()
+            C_pin.copy_(C, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(dist_mod, device)
+        with torch.cuda.stream(stream):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(e2e_steps):
+                e2e_step()
+            e1.record(stream)
+        torch.cuda.synchronize(device)
+        barrier(dist_mod, device)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist_mod, device)
+        e2e = {"value": whole_job_tflops(flop, 1, world, e2e_ms / 1e3), "unit": "TFLOPS",
+               "h2d_bytes_per_step": 4 * (M * K + K * N), "d2h_bytes_per_step": 4 * M * N,
+               "steps": e2e_steps, "ms_per_step": e2e_ms}
+        rc, site = g.gemm_f32_status(stream)
+        if rc != 0:
+            raise SystemExit("device error word %d in the e2e region" % site)
+
+    if rank != 0:
+        if dist_mod is not None:
+            dist_mod.destroy_process_group()
+        return 0
+
+    peaks, peak_src = measured_peaks()
+    t_kernel = ms_per_step / 1e3  # one launch per step
+    kernel = "ffma_gemm_kernel" if args.mode == "ffma" else "tc_gemm_kernel"
+    if args.mode == "ffma":
+        peak = FFMA_FLOP_PER_SM_CLK * torch.cuda.get_device_properties(device).multi_processor_count \
+            * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": flop / t_kernel / 1e12, "peak": peak, "unit": "TFLOP/s",
+                "peak_source": "fp32 lanes x SMs x max SM clock (%s clock)" % peak_src}
+    else:
+        peak = peaks["bf16_tflops"] * TF32_PER_BF16
+        nprod = MODE_PRODUCTS[args.mode]
+        roof = {"bound": "tensor", "achieved": nprod * flop / t_kernel / 1e12, "peak": peak,
+                "unit": "TFLOP/s",
+                "peak_source": "%s bf16 burst x nominal tf32/bf16 ratio; achieved counts the %d "
+                               "tf32 products per fp32 product" % (peak_src, nprod)}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["kernel"] = kernel
+    roof["traffic"] = recorded_traffic(kernel, args.config, args.mode)
+    roof["algorithmic_bytes"] = work_bytes
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "%s: %dx%dx%d (M,K,N) fp32 row-major, %s, seed %d" %
+                       (p.name, M, K, N, p.law, p.seed), "M": M, "K": K, "N": N, "mode": args.mode,
+                       "flags": args.flags,
+                       "l2": "flushed between steps" if flush else "inputs larger than L2",
+                       "parallelism": "replicas x%d" % world},
+            "roofline": roof, "gpu_launches": launches_per_step * args.steps}
+    if e2e is not None:
+        line["e2e"] = e2e
+    cs = clocks.summary()
+    if cs is not None:
+        line["clocks"] = cs
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = oracle_sample(A_h, B_h, args.cpu_seconds)[0]
+    print(json.dumps(line), flush=True)
+    if dist_mod is not None:
+        dist_mod.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,106 @@
+/*
+ * gemm_f32 -- row-major single-precision GEMM for NVIDIA GB300 (sm_103a).
+ *
+ * Operation (all entry points that compute):
+ *     C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j],   0 <= i < M, 0 <= j < N
+ * A is M x K, B is K x N and C is M x N, dense and row-major with leading
+ * dimensions K, N and N.  This is the element formula in the problem
+ * statement of "LeetGPU problem 2: matrix multiplication" (yekq.top, section
+ * "problem statement") and the product of "Lesson 10: shared-memory tiled
+ * GEMM" (hpc.payai.win, section 1).  C is overwritten (alpha = 1, beta = 0);
+ * it need not be initialised.  The euler0525 page computes the same product
+ * with the contraction named N; here K is always the contraction.
+ *
+ * Pointers: caller-owned DEVICE pointers (4-byte aligned), valid on the
+ * current device.  The library keeps no reference to them after the call
+ * returns and allocates no per-call memory.
+ *
+ * Streams: every call is asynchronous on `stream` (0 = legacy default
+ * stream) and never synchronises the host, like the stream-taking launcher
+ * of "Lesson 10" (section "practice task").  A device-side failure (a
+ * bounded wait that ran out) is reported later by gemm_f32_status().
+ *
+ * Sizes: any M, N, K >= 0 (M * N, M * K and K * N below 2^62).  M == 0 or
+ * N == 0 is a no-op; K == 0 writes zeros into C.  Ragged sizes are masked
+ * inside the kernels: no size needs to be a multiple of any tile.
+ *
+ * Return codes: 0 on success, else one of the negative GEMM_F32_E* codes.
+ * No entry point aborts, prints or throws.
+ */
+#ifndef GEMM_F32_H
+#define GEMM_F32_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t in the CUDA runtime headers. */
+typedef struct CUstream_st* gemm_f32_stream_t;
+
+enum gemm_f32_status_code {
+    GEMM_F32_OK = 0,
+    GEMM_F32_EINVAL = -1,   /* negative size, null pointer with work to do,
+                               C overlapping A or B, unknown mode or flag   */
+    GEMM_F32_EDEVICE = -2,  /* current device is not sm_103 (GB300), or a
+                               CUDA query failed                           */
+    GEMM_F32_ELAUNCH = -3,  /* the kernel launch (or the K == 0 memset) was
+                               refused by the CUDA runtime                  */
+    GEMM_F32_ETIMEOUT = -4  /* gemm_f32_status(): a bounded device-side wait
+                               ran out; C of that call is undefined         */
+};
+
+/* Arithmetic modes of gemm_f32_ex. */
+enum gemm_f32_mode {
+    GEMM_F32_MODE_TC3X = 0, /* default.  Tensor cores (tcgen05.mma
+                               kind::tf32): each operand is split into a
+                               TF32 high part and a TF32 low part and three
+                               products hi*hi + hi*lo + lo*hi are accumulated
+                               in fp32.  |C - exact| <= 1e-5 * (|A||B|)_ij.  */
+    GEMM_F32_MODE_FFMA = 1, /* CUDA-core fp32 fused multiply-add, register
+                               tiled.  Same 1e-5 bound.                     */
+    GEMM_F32_MODE_TC1X = 2  /* opt-in: one TF32 product on operands rounded
+                               to TF32 (nearest, ties away).  Bound 2e-3.   */
+};
+
+/* Flags of gemm_f32_ex (bitwise OR).  None changes the result beyond the
+ * mode's bound; they exist to select kernel variants for tests and tuning. */
+#define GEMM_F32_FLAG_FORCE_STAGED 0x1u  /* tensor modes: load operands with
+                                            per-thread masked loads even where
+                                            the tensor-memory-accelerator path
+                                            is possible                       */
+#define GEMM_F32_FLAG_TILE64 0x10u       /* tensor modes: output tiles of 64   */
+#define GEMM_F32_FLAG_TILE128 0x20u      /*   ... 128 or 256 rows of C (by 128 */
+#define GEMM_F32_FLAG_TILE256 0x40u      /*   columns); default: chosen by size */
+#define GEMM_F32_FLAG_ONE_TILE_PER_CTA 0x100u /* launch one CTA per output
+                                            tile instead of the persistent grid */
+
+/* C = A * B in the default mode (GEMM_F32_MODE_TC3X).  The environment
+ * variable GEMM_F32_MODE ("tc3x", "ffma" or "tc1x"), read once per process,
+ * changes the default.  Returns 0 or a negative GEMM_F32_E* code. */
+int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K,
+             gemm_f32_stream_t stream);
+
+/* C = A * B in an explicit mode with variant flags.  Returns 0 or a negative
+ * code; GEMM_F32_EINVAL for an unknown mode or flag. */
+int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K,
+                int mode, unsigned flags, gemm_f32_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns 0, GEMM_F32_ETIMEOUT if a kernel since the last call gave up
+ * on a bounded wait, or GEMM_F32_ELAUNCH if the synchronisation itself
+ * reported a CUDA error.  `site` (may be NULL) receives the code of the first
+ * wait that gave up (0 if none). */
+int gemm_f32_status(gemm_f32_stream_t stream, unsigned* site);
+
+/* Number of kernels the last successful call on this host thread launched
+ * (0 for a no-op, 1 for a GEMM, 1 for the K == 0 memset). */
+int gemm_f32_last_launches(void);
+
+/* Static version string, e.g. "gemm_f32 1.0 sm_103a". */
+const char* gemm_f32_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F32_H */

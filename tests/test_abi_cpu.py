@@ -1,0 +1,78 @@
+"""Host-side checks of the C-ABI library that need no GPU.
+
+The library must build with nvcc here, load without a GPU, export every
+function include/gemm_f32.h declares, and reject malformed requests on the
+host before it makes any CUDA call.
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from accelerator_row_major_gb300 import build as build_mod
+
+
+@pytest.fixture(scope="module")
+def g():
+    build_mod.build()
+    import accelerator_row_major_gb300 as pkg
+    return pkg
+
+
+def test_header_declares_the_entry_points(g):
+    names = g.declared_symbols()
+    assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status",
+                            "gemm_f32_last_launches", "gemm_f32_version"])
+
+
+def test_library_exports_every_declared_symbol(g):
+    lib = ctypes.CDLL(g.LIB_PATH)
+    for name in g.declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    for name in g.declared_symbols():
+        assert name in exported, name
+
+
+def test_version(g):
+    assert g.gemm_f32_version().startswith("gemm_f32 ")
+    assert "sm_103a" in g.gemm_f32_version()
+
+
+FAKE_A, FAKE_B, FAKE_C = 0x100000, 0x200000, 0x300000
+
+
+@pytest.mark.parametrize("args,mode,flags", [
+    ((FAKE_A, FAKE_B, FAKE_C, -1, 4, 4), 0, 0),          # negative M
+    ((FAKE_A, FAKE_B, FAKE_C, 4, -1, 4), 0, 0),          # negative N
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, -3), 0, 0),          # negative K
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, 4), 7, 0),           # unknown mode
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, 4), 0, 0x8000),      # unknown flag
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, 4), 0, 0x30),        # two tile widths
+    ((FAKE_A, FAKE_B, 0, 4, 4, 4), 0, 0),                # null C
+    ((0, FAKE_B, FAKE_C, 4, 4, 4), 0, 0),                # null A with K > 0
+    ((FAKE_A, FAKE_B, FAKE_A + 8, 4, 4, 4), 1, 0),       # C overlaps A
+    ((FAKE_A, FAKE_B, FAKE_B - 16, 4, 4, 4), 2, 0),      # C overlaps B
+    ((FAKE_A + 2, FAKE_B, FAKE_C, 4, 4, 4), 0, 0),       # A not 4-byte aligned
+])
+def test_malformed_requests_are_rejected_on_the_host(g, args, mode, flags):
+    assert g.gemm_f32_ex(*args, mode=mode, flags=flags) == g.GEMM_F32_EINVAL
+    assert g.gemm_f32_last_launches() == 0
+
+
+def test_empty_outputs_are_a_no_op(g):
+    # M == 0 or N == 0: nothing to write, no CUDA call, success
+    assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 0, 5, 5) == g.GEMM_F32_OK
+    assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 5, 0, 5) == g.GEMM_F32_OK
+    assert g.gemm_f32_ex(0, 0, 0, 0, 0, 0) == g.GEMM_F32_OK
+    assert g.gemm_f32_last_launches() == 0
+
+
+def test_no_gpu_is_reported_as_unsupported_device(g):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 4, 4, 4)
+    assert rc == g.GEMM_F32_EDEVICE

@@ -1,0 +1,169 @@
+"""Parity of the CUDA library (through the C ABI) with the CPU oracle.
+
+Bars: |C - C_oracle| <= tol * (|A||B|)_ij with tol 1e-5 for tc3x and ffma
+and 2e-3 for tc1x; integer inputs in [-8, 8] with K <= 512 bit-exact in
+every mode; nothing written outside C; no NaN.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from tests._gpu import (TOL, assert_bit_exact, assert_close, max_rel_err, oracle_full, run_abi,
+                        sample_indices)
+
+pytestmark = pytest.mark.gpu
+
+MODES = ["tc3x", "ffma", "tc1x"]
+FLAG_STAGED = 0x1
+FLAG_TILE = {64: 0x10, 128: 0x20, 256: 0x40}
+FLAG_ONE_TILE = 0x100
+
+
+@pytest.fixture(scope="module")
+def small_problems():
+    out = {}
+    for name in ("c1", "c1int", "c2", "c3"):
+        A, B = workloads.problem_inputs(name)
+        C, absAB = oracle_full(A, B)
+        out[name] = (A, B, C, absAB)
+    return out
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+def test_small_configs_within_tolerance(small_problems, name, mode):
+    A, B, Co, absAB = small_problems[name]
+    C, _ = run_abi(A, B, mode)
+    assert_close(C, Co, absAB, TOL[mode], "%s/%s" % (name, mode))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_integer_config_bit_exact(small_problems, mode):
+    A, B, Co, _ = small_problems["c1int"]
+    C, _ = run_abi(A, B, mode)
+    assert_bit_exact(C, Co, "c1int/%s" % mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("flags", [0, FLAG_STAGED])
+def test_integer_k512_bit_exact(mode, flags):
+    # the regular size with integer values: every partial sum is exact
+    A, B = workloads.make_inputs(1024, 512, 1024, "int8", 11)
+    Co, _ = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode, flags)
+    assert_bit_exact(C, Co, "int 1024x512x1024/%s/%d" % (mode, flags))
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("tm", [64, 128, 256])
+@pytest.mark.parametrize("staged", [False, True])
+def test_every_tensor_variant_on_ragged_and_regular(small_problems, mode, tm, staged):
+    for name in ("c3", "c2"):
+        A, B, Co, absAB = small_problems[name]
+        flags = FLAG_TILE[tm] | (FLAG_STAGED if staged else 0)
+        C, _ = run_abi(A, B, mode, flags)
+        assert_close(C, Co, absAB, TOL[mode], "%s/%s/tm%d/staged%d" % (name, mode, tm, staged))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_one_tile_per_cta_grid(small_problems, mode):
+    A, B, Co, absAB = small_problems["c3"]
+    C, _ = run_abi(A, B, mode, FLAG_ONE_TILE)
+    assert_close(C, Co, absAB, TOL[mode], "c3/one-tile/%s" % mode)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_deterministic(small_problems, mode):
+    A, B, _, _ = small_problems["c3"]
+    _, outs = run_abi(A, B, mode, repeats=2)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+
+
+# sizes around tile and swizzle edges: 1, the vector width, 8, 16, 32,
+# 64, 128, 256 and their neighbours
+EDGE = [1, 2, 3, 4, 5, 7, 8, 15, 17, 31, 33, 63, 65, 127, 129, 255, 257]
+
+
+def _edge_cases(seed, count):
+    rng = np.random.default_rng(seed)
+    cases = set()
+    while len(cases) < count:
+        cases.add(tuple(int(x) for x in rng.choice(EDGE, 3)))
+    return sorted(cases)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_edge_sweep(mode):
+    for (M, K, N) in _edge_cases(5 + MODES.index(mode), 40):
+        A, B = workloads.make_inputs(M, K, N, "uniform", M * 7 + K * 3 + N)
+        Co, absAB = oracle_full(A, B)
+        C, _ = run_abi(A, B, mode)
+        assert_close(C, Co, absAB, TOL[mode], "edge %dx%dx%d/%s" % (M, K, N, mode))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("offsets", [(1, 0, 0), (0, 1, 0), (0, 0, 1), (3, 2, 1)])
+def test_misaligned_base_pointers(mode, offsets):
+    A, B = workloads.make_inputs(300, 264, 200, "uniform", 77)
+    Co, absAB = oracle_full(A, B)
+    oa, ob, oc = offsets
+    C, _ = run_abi(A, B, mode, offset_a=oa, offset_b=ob, offset_c=oc)
+    assert_close(C, Co, absAB, TOL[mode], "misaligned %s/%s" % (offsets, mode))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_k_zero_writes_zeros(mode):
+    A = np.zeros((70, 0), np.float32)
+    B = np.zeros((0, 90), np.float32)
+    C, _ = run_abi(A, B, mode)
+    assert C.shape == (70, 90) and not C.any()
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 513, 300), (300, 513, 1), (1, 1, 4096),
+                                   (129, 1, 257), (2, 3000, 2)])
+def test_degenerate_shapes(mode, shape):
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "normal", sum(shape))
+    Co, absAB = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode)
+    assert_close(C, Co, absAB, TOL[mode], "degenerate %s/%s" % (shape, mode))
+
+
+def test_closed_forms_on_gpu():
+    # A = I gives B exactly in every mode for TF32-exact values; ones give
+    # column sums of small integers exactly
+    n = 200
+    B = workloads.make_inputs(1, n, 150, "int8", 3)[1]
+    for mode in MODES:
+        C, _ = run_abi(np.eye(n, dtype=np.float32), B, mode)
+        assert_bit_exact(C, B, "identity/%s" % mode)
+        C, _ = run_abi(np.ones((33, n), np.float32), B, mode)
+        assert_bit_exact(C, np.broadcast_to(B.sum(axis=0, dtype=np.float64).astype(np.float32), (33, 150)),
+                         "ones/%s" % mode)
+
+
+@pytest.mark.parametrize("name", ["c4", "c5b", "c5c", "c5a"])
+@pytest.mark.parametrize("mode", ["tc3x", "ffma"])
+def test_large_configs_sampled(name, mode):
+    """Full-size problems in the default launch configuration: sampled
+    entries against the oracle computed one by one."""
+    A, B = workloads.problem_inputs(name)
+    M, K = A.shape
+    N = B.shape[1]
+    C, _ = run_abi(A, B, mode)
+    rows, cols = sample_indices(M, N, 3000, 1234)
+    vals, absv = oracle.gemm_entries(A, B, rows, cols)
+    got = C[rows, cols]
+    assert_close(got[None, :], vals[None, :], absv[None, :], TOL[mode], "%s/%s" % (name, mode))
+    assert not np.isnan(C).any()
+    print("%s/%s max err/absAB %.3e" % (name, mode, max_rel_err(got, vals, absv)))
+
+
+def test_large_config_tc1x_sampled():
+    A, B = workloads.problem_inputs("c4")
+    C, _ = run_abi(A, B, "tc1x")
+    rows, cols = sample_indices(A.shape[0], B.shape[1], 2000, 99)
+    vals, absv = oracle.gemm_entries(A, B, rows, cols)
+    assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc1x"], "c4/tc1x")
