@@ -198,7 +198,14 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]
       : "r"(taddr));
 }
 
-// Each thread of the warp writes 16 / 32 consecutive 32-bit columns of its lane.
+// Each thread of the warp writes 8 / 16 / 32 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st_8cols(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+      : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -271,12 +278,15 @@ __device__ __forceinline__ uint32_t tf32_round_bits(uint32_t x) {
   return (x + 0x1000u) & 0xFFFFE000u;
 }
 
-// x = hi + lo exactly (x - hi is exact: hi is within a factor of two of x);
-// lo is then rounded to TF32 as well, so both parts are exact TF32 values.
-__device__ __forceinline__ void tf32_split(uint32_t x, uint32_t& hi, uint32_t& lo) {
-  hi = tf32_round_bits(x);
-  const float r = __fsub_rn(__uint_as_float(x), __uint_as_float(hi));
-  lo = tf32_round_bits(__float_as_uint(r));
+// Low part for an operand whose high part is the raw fp32 value: the tensor
+// core reads a 32-bit operand as TF32 by dropping its 13 low mantissa bits
+// (measured on GB300 for both shared-memory and tensor-memory operands), so
+// the high part it sees is trunc(x) = x with those bits cleared.  The rest,
+// x - trunc(x), is exact in fp32 and is rounded to the nearest TF32 value so
+// that the tensor core reads it unchanged.
+__device__ __forceinline__ uint32_t tf32_lo_of_truncated(uint32_t x) {
+  const float r = __fsub_rn(__uint_as_float(x), __uint_as_float(x & 0xFFFFE000u));
+  return tf32_round_bits(__float_as_uint(r));
 }
 
 }  // namespace gemm_f32_dev

@@ -21,13 +21,15 @@
 // therefore accumulates the transposed tile, D[n][m] = C[m][n], which also
 // makes the epilogue's stores coalesced (lane t writes column n0 + t).
 //
-// Roles inside one persistent CTA (one CTA per SM, 12 warps):
+// Roles inside one persistent CTA (one CTA per SM, 16 warps):
 //   warp 0        TMA producer: A tile [TM x BK] (swizzled) and B tile
 //                 [BK x 128] per K phase into stage s
 //   warp 1        TMEM allocator and MMA issuer (one thread)
 //   warps 4..7    epilogue: TMEM -> registers -> C (masked, coalesced)
-//   warps 8..11   transform: A tile -> TF32 hi (in place) and lo in shared
-//                 memory; B tile -> TF32 hi/lo of its transpose in TMEM.
+//   warps 8..15   transform: A tile -> TF32 hi (in place) and lo in shared
+//                 memory; B tile -> TF32 hi/lo of its transpose in TMEM
+//                 (warps w and w+4 share TMEM lanes 32(w%4).., each taking
+//                 half of the tile's K rows).
 //                 On the staged path (operands TMA cannot address) these
 //                 warps load both tiles from global memory themselves.
 // Every role walks the same tile sequence and the same K-phase count, so
@@ -53,11 +55,11 @@ using namespace gemm_f32_dev;
 namespace {
 
 constexpr int kTN = 128;                     // columns of C per tile = TMEM lanes = MMA M
-constexpr int kWarps = 12;                   // see role table above
+constexpr int kWarps = 16;                   // see role table above
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpilogueWarp0 = 4;
 constexpr int kTransformWarp0 = 8;
-constexpr int kTransformThreads = 128;
+constexpr int kTransformThreads = 256;       // two warps per TMEM lane quarter
 constexpr int kEpilogueThreads = 128;
 constexpr int kSmemLimit = 232448;           // opt-in dynamic shared memory per block
 constexpr int kTmemCols = 512;
@@ -103,15 +105,29 @@ __device__ __forceinline__ uint32_t swizzle(uint32_t o, uint32_t mask) {
   return o ^ (((o >> 7) & mask) << 4);
 }
 
-template <int BK>
-__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t (&v)[BK]);
+// The operand parts the tensor core is given for one fp32 element: with
+// three products, hi = the raw bits (read as trunc(x)) and lo = the rounded
+// remainder; with one product, hi = x rounded to the nearest TF32 value.
+template <int NPROD>
+__device__ __forceinline__ void split_operand(uint32_t x, uint32_t& hi, uint32_t& lo) {
+  if (NPROD == 3) {
+    hi = x;
+    lo = tf32_lo_of_truncated(x);
+  } else {
+    hi = tf32_round_bits(x);
+    lo = 0u;
+  }
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t (&v)[NC]);
+template <>
+__device__ __forceinline__ void tmem_store_cols<8>(uint32_t taddr, const uint32_t (&v)[8]) {
+  tmem_st_8cols(taddr, v);
+}
 template <>
 __device__ __forceinline__ void tmem_store_cols<16>(uint32_t taddr, const uint32_t (&v)[16]) {
   tmem_st_16cols(taddr, v);
-}
-template <>
-__device__ __forceinline__ void tmem_store_cols<32>(uint32_t taddr, const uint32_t (&v)[32]) {
-  tmem_st_32cols(taddr, v);
 }
 
 template <int TM, int BK, int NPROD, bool TMA>
@@ -283,8 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kTransformWarp0) {
     // ------------------------------------------------------------ transform
-    const int tt = threadIdx.x - kTransformWarp0 * 32;   // = this thread's TMEM lane
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(tt & ~31) << 16);
+    constexpr int KH = BK / 2;                            // K rows of B per thread
+    const int tt = threadIdx.x - kTransformWarp0 * 32;    // 0 .. 255
+    const int col = tt & 127;                             // = this thread's TMEM lane
+    const int kh0 = (tt >> 7) * KH;                       // first K row of its half
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(col & ~31) << 16);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -303,27 +322,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        uint32_t bh[BK], bl[BK];
+        uint32_t bh[KH], bl[KH];
         if (TMA) {
-          // A: split in place (layout preserving), lo to its own buffer
+          // A: three products read the raw tile as the high part; only the
+          // low part is written.  One product rounds the tile in place.
           uint4* const hi = reinterpret_cast<uint4*>(st);
           uint4* const lo = reinterpret_cast<uint4*>(st + Cfg::A_BYTES);
 #pragma unroll 4
           for (int i = tt; i < Cfg::A_BYTES / 16; i += kTransformThreads) {
             const uint4 x = hi[i];
-            uint4 h, l;
-            tf32_split(x.x, h.x, l.x);
-            tf32_split(x.y, h.y, l.y);
-            tf32_split(x.z, h.z, l.z);
-            tf32_split(x.w, h.w, l.w);
-            hi[i] = h;
-            if (NPROD == 3) lo[i] = l;
+            if (NPROD == 3) {
+              lo[i] = make_uint4(tf32_lo_of_truncated(x.x), tf32_lo_of_truncated(x.y),
+                                 tf32_lo_of_truncated(x.z), tf32_lo_of_truncated(x.w));
+            } else {
+              hi[i] = make_uint4(tf32_round_bits(x.x), tf32_round_bits(x.y), tf32_round_bits(x.z),
+                                 tf32_round_bits(x.w));
+            }
           }
-          // B: column tt of the raw tile
+          // B: column `col` of the raw tile, K rows kh0 .. kh0+KH-1
           const uint32_t* braw =
               reinterpret_cast<const uint32_t*>(st + Cfg::A_BYTES + Cfg::A_LO_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK; ++k) tf32_split(braw[k * kTN + tt], bh[k], bl[k]);
+          for (int k = 0; k < KH; ++k) split_operand<NPROD>(braw[(kh0 + k) * kTN + col], bh[k], bl[k]);
         } else {
           const int m0 = c.tm * TM, n0 = c.tn * kTN, k0 = kt * BK;
           // A tile: row r, column k; lanes run along k (coalesced)
@@ -335,25 +355,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
                                    : 0u;
             uint32_t h, l;
-            tf32_split(x, h, l);
+            split_operand<NPROD>(x, h, l);
             const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
             *reinterpret_cast<uint32_t*>(st + o) = h;
             if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
           }
-          // B tile: column n0 + tt, rows k0 .. k0+BK-1 (lanes along n: coalesced)
-          const int gn = n0 + tt;
+          // B tile: column n0 + col, K rows of this thread's half (lanes along n: coalesced)
+          const int gn = n0 + col;
 #pragma unroll
-          for (int k = 0; k < BK; ++k) {
-            const int gk = k0 + k;
+          for (int k = 0; k < KH; ++k) {
+            const int gk = k0 + kh0 + k;
             const uint32_t x = (gn < p.N && gk < p.K)
                                    ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
                                    : 0u;
-            tf32_split(x, bh[k], bl[k]);
+            split_operand<NPROD>(x, bh[k], bl[k]);
           }
         }
-        const uint32_t bt = lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS);
-        tmem_store_cols<BK>(bt, bh);
-        if (NPROD == 3) tmem_store_cols<BK>(bt + BK, bl);
+        const uint32_t bt =
+            lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS + kh0);
+        tmem_store_cols<KH>(bt, bh);
+        if (NPROD == 3) tmem_store_cols<KH>(bt + BK, bl);
         tmem_wait_st();
         fence_proxy_async_smem();  // A hi/lo: generic-proxy writes -> tensor-core reads
         tc_fence_before_sync();
@@ -442,8 +463,10 @@ int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const CUtensorMap& m
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Tile height TM: the one whose persistent schedule gives the busiest SM the
-// least work (rounds x TM, plus a per-tile overhead), preferring taller tiles
-// on a tie (each B panel is then split fewer times).
+// least time, counting rounds of tiles x TM / (relative efficiency of that
+// tile height).  Shorter tiles repeat the per-stage transform of B for fewer
+// rows of A and keep the tensor pipe less busy; the efficiencies are the
+// measured 8192^3 throughputs of TM = 128 and 64 relative to TM = 256.
 int choose_tm(const GemmArgs& g) {
   if (g.flags & GEMM_F32_FLAG_TILE64) return 64;
   if (g.flags & GEMM_F32_FLAG_TILE128) return 128;
@@ -451,13 +474,15 @@ int choose_tm(const GemmArgs& g) {
   const long tn = ceil_div(g.N, kTN);
   long best_cost = -1;
   int best = 256;
-  for (int tm : {256, 128, 64}) {
-    const long tiles = tn * ceil_div(g.M, tm);
+  const int tms[3] = {256, 128, 64};
+  const long eff_pct[3] = {100, 76, 43};
+  for (int i = 0; i < 3; ++i) {
+    const long tiles = tn * ceil_div(g.M, tms[i]);
     const long rounds = (tiles + g.num_sms - 1) / g.num_sms;
-    const long cost = rounds * (tm + 16);
+    const long cost = rounds * tms[i] * 100 / eff_pct[i];
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
-      best = tm;
+      best = tms[i];
     }
   }
   return best;
