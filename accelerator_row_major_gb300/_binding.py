@@ -30,6 +30,7 @@ FLAG_TILE64 = 0x10
 FLAG_TILE128 = 0x20
 FLAG_TILE256 = 0x40
 FLAG_ONE_TILE_PER_CTA = 0x100
+FLAG_TEST_DROP_COPY = 0x1000
 
 _ERRORS = {
     GEMM_F32_EINVAL: "invalid argument",

@@ -84,7 +84,7 @@ bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
 
 constexpr unsigned kKnownFlags = GEMM_F32_FLAG_FORCE_STAGED | GEMM_F32_FLAG_TILE64 |
                                  GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
-                                 GEMM_F32_FLAG_ONE_TILE_PER_CTA;
+                                 GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_TEST_DROP_COPY;
 
 }  // namespace
 

@@ -71,6 +71,7 @@ struct TcParams {
   float* C;
   int M, N, K;
   int tiles_m, tiles_n, k_iters;
+  int drop_first_copy;  // testing only: CTA 0 skips its first copy
   unsigned* err;
 };
 
@@ -199,6 +200,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t st = base + s * Cfg::STAGE_BYTES;
+          if (p.drop_first_copy && blockIdx.x == 0 && t == 0 && kt == 0) {
+            // test hook: this stage is never filled, so every role that
+            // depends on it runs into its bounded wait
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(full_bar(s), Cfg::A_BYTES + Cfg::B_RAW_BYTES);
           armed |= 1u << s;
           last_ph = (last_ph & ~(1u << s)) | (ph << s);
@@ -504,6 +514,7 @@ int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) 
   p.tiles_m = ceil_div(g.M, tm);
   p.tiles_n = ceil_div(g.N, kTN);
   p.k_iters = ceil_div(g.K, bk);
+  p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
   const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;

@@ -73,6 +73,14 @@ enum gemm_f32_mode {
 #define GEMM_F32_FLAG_TILE256 0x40u      /*   columns); default: chosen by size */
 #define GEMM_F32_FLAG_ONE_TILE_PER_CTA 0x100u /* launch one CTA per output
                                             tile instead of the persistent grid */
+#define GEMM_F32_FLAG_TEST_DROP_COPY 0x1000u /* testing only, tensor modes on
+                                            the TMA path: CTA 0 never issues
+                                            its first operand copy, so its
+                                            bounded waits run out (about 2 s)
+                                            and gemm_f32_status() returns
+                                            GEMM_F32_ETIMEOUT.  C is undefined
+                                            after such a call.  Ignored by the
+                                            FFMA mode, which has no waits.    */
 
 /* C = A * B in the default mode (GEMM_F32_MODE_TC3X).  The environment
  * variable GEMM_F32_MODE ("tc3x", "ffma" or "tc1x"), read once per process,

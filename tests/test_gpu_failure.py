@@ -1,0 +1,50 @@
+"""Failure detection on the GPU without a fault: a bounded wait that runs out.
+
+The test flag makes CTA 0's producer skip its first operand copy, so the
+waits that depend on it give up after their 2 s budget.  The call must
+return, gemm_f32_status() must report GEMM_F32_ETIMEOUT with a site code,
+and the context must stay usable for the next call.
+"""
+import time
+
+import numpy as np
+import pytest
+
+import workloads
+from tests._gpu import TOL, assert_close, lib, oracle_full, run_abi
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+def test_lost_copy_reports_timeout_and_context_survives(mode):
+    import torch
+
+    g = lib()
+    A, B = workloads.make_inputs(256, 64, 256, "uniform", 8)
+    dev = torch.device("cuda:0")
+    At = torch.from_numpy(A).to(dev)
+    Bt = torch.from_numpy(B).to(dev)
+    C = torch.empty((256, 256), dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    t0 = time.time()
+    rc = g.gemm_f32_ex(At, Bt, C, 256, 256, 64, mode, g.FLAG_TEST_DROP_COPY, s)
+    assert rc == g.GEMM_F32_OK
+    st, site = g.gemm_f32_status(s)
+    elapsed = time.time() - t0
+    assert st == g.GEMM_F32_ETIMEOUT
+    assert site in (1, 2, 3, 4, 5, 6, 7, 8)
+    assert 1.5 < elapsed < 30.0
+    # the error word was cleared by the read, and the context still works
+    assert g.gemm_f32_status(s) == (g.GEMM_F32_OK, 0)
+    Co, absAB = oracle_full(A, B)
+    C2, _ = run_abi(A, B, mode)
+    assert_close(C2, Co, absAB, TOL[mode], "after timeout/%s" % mode)
+
+
+def test_ffma_ignores_the_test_flag():
+    g = lib()
+    A, B = workloads.make_inputs(200, 64, 136, "uniform", 9)
+    Co, absAB = oracle_full(A, B)
+    C, _ = run_abi(A, B, "ffma", g.FLAG_TEST_DROP_COPY)
+    assert_close(C, Co, absAB, TOL["ffma"], "ffma with test flag")
