@@ -10,10 +10,11 @@ streams.
     g.gemm_f32(A, B, C, M, N, K, stream)   # the C-ABI call, same arguments
 """
 from ._binding import (FLAG_FORCE_STAGED, FLAG_TILE64, FLAG_TILE128, FLAG_TILE256,  # noqa: F401
-                       FLAG_ONE_TILE_PER_CTA, FLAG_TEST_DROP_COPY, GEMM_F32_EDEVICE, GEMM_F32_EINVAL,
+                       FLAG_NO_SPLIT_K, FLAG_ONE_TILE_PER_CTA, FLAG_TEST_DROP_COPY, GEMM_F32_EDEVICE, GEMM_F32_EINVAL,
                        GEMM_F32_ELAUNCH, GEMM_F32_ETIMEOUT, GEMM_F32_OK, LIB_PATH, MODE_FFMA,
                        MODE_TC1X, MODE_TC3X, MODES, GemmError, check, declared_symbols,
-                       gemm_f32, gemm_f32_ex, gemm_f32_last_launches, gemm_f32_status,
+                       gemm_f32, gemm_f32_ex, gemm_f32_last_launches, gemm_f32_release,
+                       gemm_f32_status,
                        gemm_f32_version)
 
 

@@ -30,6 +30,7 @@ FLAG_TILE64 = 0x10
 FLAG_TILE128 = 0x20
 FLAG_TILE256 = 0x40
 FLAG_ONE_TILE_PER_CTA = 0x100
+FLAG_NO_SPLIT_K = 0x200
 FLAG_TEST_DROP_COPY = 0x1000
 
 _ERRORS = {
@@ -59,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_status.restype = ci
     lib.gemm_f32_last_launches.argtypes = []
     lib.gemm_f32_last_launches.restype = ci
+    lib.gemm_f32_release.argtypes = []
+    lib.gemm_f32_release.restype = ci
     lib.gemm_f32_version.argtypes = []
     lib.gemm_f32_version.restype = ctypes.c_char_p
     return lib
@@ -120,6 +123,11 @@ def gemm_f32_status(stream=None):
 
 def gemm_f32_last_launches() -> int:
     return lib().gemm_f32_last_launches()
+
+
+def gemm_f32_release() -> int:
+    """Frees the current device's workspaces (synchronises the device)."""
+    return lib().gemm_f32_release()
 
 
 def gemm_f32_version() -> str:

@@ -22,6 +22,7 @@ enum WaitSite : unsigned {
   kSiteEpilogueFull = 6,    // epilogue waiting for a finished accumulator
   kSiteDrainMma = 7,        // teardown: waiting for the last MMAs
   kSiteDrainTma = 8,        // teardown: waiting for copies in flight
+  kSitePendingOverflow = 9, // split-tail bookkeeping exceeded its bound
 };
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

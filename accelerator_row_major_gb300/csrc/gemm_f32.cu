@@ -8,6 +8,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "../../include/gemm_f32.h"
 #include "launch.h"
@@ -20,11 +21,19 @@ __device__ unsigned g_error_word;
 
 constexpr int kMaxDevices = 64;
 
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  bool dirty = false;             // a kernel gave up on a wait since last use
+};
+
 struct DeviceState {
   std::once_flag once;
   int status = GEMM_F32_EDEVICE;  // GEMM_F32_OK once set up
   int num_sms = 0;
   unsigned* err = nullptr;        // device address of g_error_word
+  std::mutex ws_mu;
+  std::unordered_map<cudaStream_t, Workspace> ws;  // one per stream
 };
 
 DeviceState g_devices[kMaxDevices];
@@ -84,9 +93,45 @@ bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
 
 constexpr unsigned kKnownFlags = GEMM_F32_FLAG_FORCE_STAGED | GEMM_F32_FLAG_TILE64 |
                                  GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
-                                 GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_TEST_DROP_COPY;
+                                 GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K |
+                                 GEMM_F32_FLAG_TEST_DROP_COPY;
 
 }  // namespace
+
+void* gemm_f32_impl::acquire_workspace(int device, cudaStream_t stream, size_t bytes,
+                                       int* must_clear) {
+  *must_clear = 0;
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  DeviceState& st = g_devices[device];
+  std::lock_guard<std::mutex> lock(st.ws_mu);
+  Workspace& w = st.ws[stream];
+  if (w.bytes < bytes) {
+    if (w.ptr) {
+      (void)cudaFree(w.ptr);   // synchronises the device: no kernel still uses it
+      w.ptr = nullptr;
+      w.bytes = 0;
+    }
+    const size_t want = (bytes + (1u << 20) - 1) & ~static_cast<size_t>((1u << 20) - 1);
+    void* p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    if (cudaMemset(p, 0, want) != cudaSuccess) {
+      (void)cudaGetLastError();
+      (void)cudaFree(p);
+      return nullptr;
+    }
+    w.ptr = p;
+    w.bytes = want;
+    w.dirty = false;
+  }
+  if (w.dirty) {
+    *must_clear = 1;
+    w.dirty = false;
+  }
+  return w.ptr;
+}
 
 extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
                            unsigned flags, gemm_f32_stream_t stream_handle) {
@@ -166,7 +211,27 @@ extern "C" int gemm_f32_status(gemm_f32_stream_t stream_handle, unsigned* site) 
     return GEMM_F32_ELAUNCH;
   }
   if (site) *site = word;
+  if (word) {  // a kernel may have left split-tail counters half counted
+    std::lock_guard<std::mutex> lock(st->ws_mu);
+    for (auto& kv : st->ws) kv.second.dirty = true;
+  }
   return word ? GEMM_F32_ETIMEOUT : GEMM_F32_OK;
+}
+
+extern "C" int gemm_f32_release(void) {
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  std::lock_guard<std::mutex> lock(st->ws_mu);
+  int rc = GEMM_F32_OK;
+  if (cudaDeviceSynchronize() != cudaSuccess) {
+    (void)cudaGetLastError();
+    rc = GEMM_F32_ELAUNCH;
+  }
+  for (auto& kv : st->ws)
+    if (kv.second.ptr) (void)cudaFree(kv.second.ptr);
+  st->ws.clear();
+  return rc;
 }
 
 extern "C" int gemm_f32_last_launches(void) { return t_last_launches; }

@@ -17,6 +17,14 @@ struct GemmArgs {
   unsigned flags;       // GEMM_F32_FLAG_* bits
 };
 
+// The library's workspace for `stream` on `device` (one per device and
+// stream), grown to at least `bytes` with cudaMalloc when needed (which
+// synchronises the device) and zeroed when allocated.  *must_clear is set
+// when the caller must re-zero the split-tail counters before using it (a
+// kernel on this device gave up on a bounded wait since it was last used).
+// Returns nullptr if the memory cannot be had; the caller then does without.
+void* acquire_workspace(int device, cudaStream_t stream, size_t bytes, int* must_clear);
+
 // Tensor-core path (tcgen05.mma kind::tf32).  nprod = 3 (split hi/lo, three
 // products) or 1 (operands rounded to TF32, one product).  Returns 0 or a
 // negative GEMM_F32_E* code.  *launches receives the kernels launched.

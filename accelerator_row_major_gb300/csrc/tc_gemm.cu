@@ -32,9 +32,18 @@
 //                 half of the tile's K rows).
 //                 On the staged path (operands TMA cannot address) these
 //                 warps load both tiles from global memory themselves.
-// Every role walks the same tile sequence and the same K-phase count, so
-// no role leaves a barrier phase unfinished (the uniform-control rule of
-// "Lesson 10", section 3).
+// Every role walks the same list of work items (below) and the same K-phase
+// count per item, so no role leaves a barrier phase unfinished (the
+// uniform-control rule of "Lesson 10", section 3).
+//
+// Work list of CTA c (grid G): first whole tiles c, c+G, ... of the leading
+// full waves; then, when the tile count is not a multiple of G, an equal
+// share of the remaining tiles' K iterations (the tail is cut along K, so
+// every CTA finishes at about the same time).  A CTA that computes only part
+// of a tile's K range writes its partial tile to a workspace and bumps the
+// tile's counter; the CTA that arrives last adds all partials in segment
+// order (fixed, so the result does not depend on which CTA is last) and
+// writes C.  No CTA waits for another.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -61,9 +70,17 @@ constexpr int kEpilogueWarp0 = 4;
 constexpr int kTransformWarp0 = 8;
 constexpr int kTransformThreads = 256;       // two warps per TMEM lane quarter
 constexpr int kEpilogueThreads = 128;
+constexpr int kEpilogueBarrier = 1;          // named barrier of the epilogue warps
 constexpr int kSmemLimit = 232448;           // opt-in dynamic shared memory per block
 constexpr int kTmemCols = 512;
 constexpr int kRasterGroup = 8;              // tile-rows per L2 group
+constexpr int kMinSplitIters = 64;           // least K iterations per CTA in the split tail
+constexpr int kMaxPending = 8;               // split tiles one CTA may have to reduce
+// Split-tail counters live at the start of the workspace, one per tail tile
+// (a tail has fewer tiles than there are SMs), at the same place for every
+// problem, so the zeros the last CTA of each tile leaves behind are seen by
+// the next call whatever its shape.
+constexpr size_t kCounterBytes = 4096;
 
 struct TcParams {
   const float* A;
@@ -71,8 +88,72 @@ struct TcParams {
   float* C;
   int M, N, K;
   int tiles_m, tiles_n, k_iters;
-  int drop_first_copy;  // testing only: CTA 0 skips its first copy
+  int dp_tiles;          // tiles 0 .. dp_tiles-1 are computed whole, round robin
+  int sk_ctas;           // CTAs 0 .. sk_ctas-1 share the K iterations of the rest
+  long long sk_work;     // (tiles - dp_tiles) * k_iters
+  int max_seg;           // most CTAs sharing one tail tile
+  float* partials;       // [tail tile][max_seg][TM][128] fp32
+  unsigned* counters;    // [tail tile]: partials written so far (zero between calls)
+  int drop_first_copy;   // testing only: CTA 0 skips its first copy
   unsigned* err;
+};
+
+// One unit of a CTA's work: K iterations [k0, k1) of one output tile.
+struct WorkItem {
+  int tile, k0, k1;
+  int tail;        // index among the split tiles, or -1 for a whole tile
+  int seg, nseg;   // this CTA's position among the CTAs sharing the tile
+};
+
+__host__ __device__ __forceinline__ long long sk_start(long long c, long long ctas, long long work) {
+  return c * work / ctas;
+}
+// CTA whose share of the split K iterations contains iteration x
+__host__ __device__ __forceinline__ int sk_owner(long long x, long long ctas, long long work) {
+  return static_cast<int>(((x + 1) * ctas - 1) / work);
+}
+
+// The work list of one CTA, walked identically by every role.
+struct WorkList {
+  int next_dp;
+  long long x, x_end;
+
+  __device__ __forceinline__ explicit WorkList(const TcParams& p) {
+    next_dp = blockIdx.x;
+    x = x_end = 0;
+    if (static_cast<int>(blockIdx.x) < p.sk_ctas) {
+      x = sk_start(blockIdx.x, p.sk_ctas, p.sk_work);
+      x_end = sk_start(blockIdx.x + 1, p.sk_ctas, p.sk_work);
+    }
+  }
+
+  __device__ __forceinline__ bool next(const TcParams& p, WorkItem& w) {
+    if (next_dp < p.dp_tiles) {
+      w.tile = next_dp;
+      w.k0 = 0;
+      w.k1 = p.k_iters;
+      w.tail = -1;
+      w.seg = 0;
+      w.nseg = 1;
+      next_dp += gridDim.x;
+      return true;
+    }
+    if (x < x_end) {
+      const long long ki = p.k_iters;
+      const int i = static_cast<int>(x / ki);
+      w.tile = p.dp_tiles + i;
+      w.tail = i;
+      w.k0 = static_cast<int>(x - i * ki);
+      w.k1 = static_cast<int>(min(ki, w.k0 + (x_end - x)));
+      const int first = sk_owner(i * ki, p.sk_ctas, p.sk_work);
+      const int last = sk_owner((i + 1) * ki - 1, p.sk_ctas, p.sk_work);
+      w.seg = static_cast<int>(blockIdx.x) - first;
+      w.nseg = last - first + 1;
+      x += w.k1 - w.k0;
+      return true;
+    }
+    return false;
+  }
 };
 
 template <int TM, int BK, int NPROD>
@@ -131,6 +212,26 @@ __device__ __forceinline__ void tmem_store_cols<16>(uint32_t taddr, const uint32
   tmem_st_16cols(taddr, v);
 }
 
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync %0, %1;" ::"r"(kEpilogueBarrier), "r"(kEpilogueThreads) : "memory");
+}
+
+// True on every epilogue thread iff `v` is true on all of them (a barrier:
+// every epilogue thread reaches it after its own bounded wait, so a wait
+// that runs out on some threads and not on others cannot split the group).
+__device__ __forceinline__ bool epilogue_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(kEpilogueBarrier), "r"(kEpilogueThreads)
+      : "memory");
+  return r != 0;
+}
+
 template <int TM, int BK, int NPROD, bool TMA>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -151,11 +252,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto acce_bar = [&](int b) { return bars + 8u * (3 * S + NACC + b); };  // accumulator b drained
   const uint32_t drain_bar = bars + 8u * (3 * S + 2 * NACC);
   const uint32_t tmem_slot = drain_bar + 8u;
+  // split tiles this CTA published last, reduced after the work list
+  volatile int* const pending_count = reinterpret_cast<volatile int*>(base_ptr + (tmem_slot + 8u - base));
+  WorkItem* const pending = reinterpret_cast<WorkItem*>(base_ptr + (tmem_slot + 16u - base));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    *pending_count = 0;
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(ready_bar(s), kTransformThreads);
@@ -181,9 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
 
-  const int num_tiles = p.tiles_m * p.tiles_n;
-  const int k_iters = p.k_iters;
-
+  WorkItem w;
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (TMA && lane == 0) {
@@ -192,23 +295,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t armed = 0;    // bit s: stage s was armed at least once
       uint32_t last_ph = 0;  // bit s: parity of the last arming of stage s
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
-        for (int kt = 0; kt < k_iters; ++kt) {
+      bool first = true;
+      WorkList list(p);
+      while (ok && list.next(p, w)) {
+        const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+        for (int kt = w.k0; kt < w.k1; ++kt) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteProducerEmpty)) {
             ok = false;
             break;
           }
           const uint32_t st = base + s * Cfg::STAGE_BYTES;
-          if (p.drop_first_copy && blockIdx.x == 0 && t == 0 && kt == 0) {
+          if (p.drop_first_copy && blockIdx.x == 0 && first) {
             // test hook: this stage is never filled, so every role that
             // depends on it runs into its bounded wait
+            first = false;
             if (++s == S) {
               s = 0;
               ph ^= 1u;
             }
             continue;
           }
+          first = false;
           mbar_arrive_expect_tx(full_bar(s), Cfg::A_BYTES + Cfg::B_RAW_BYTES);
           armed |= 1u << s;
           last_ph = (last_ph & ~(1u << s)) | (ph << s);
@@ -233,11 +340,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       int acc = 0;
       uint32_t acc_ph = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      WorkList list(p);
+      while (ok && list.next(p, w)) {
         if (!mbar_wait(acce_bar(acc), acc_ph ^ 1u, p.err, kSiteMmaAccEmpty)) break;
         tc_fence_after_sync();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TM);
-        for (int kt = 0; kt < k_iters; ++kt) {
+        for (int kt = w.k0; kt < w.k1; ++kt) {
           if (!mbar_wait(ready_bar(s), ph, p.err, kSiteMmaReady)) {
             ok = false;
             break;
@@ -248,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint64_t a_hi = smem_desc(st + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
-            mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_hi, idesc, (kt | kk) != 0 ? 1u : 0u);
+            mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_hi, idesc, (kt > w.k0 || kk > 0) ? 1u : 0u);
             if (NPROD == 3) {
               const uint64_t a_lo =
                   smem_desc(st + Cfg::A_BYTES + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
@@ -276,28 +384,54 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
+    const int nl = q * 32 + lane;  // this thread's column within the tile
     int acc = 0;
     uint32_t acc_ph = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
-      if (!mbar_wait(accf_bar(acc), acc_ph, p.err, kSiteEpilogueFull)) break;
+    WorkList list(p);
+    while (list.next(p, w)) {
+      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      if (!epilogue_all(mbar_wait(accf_bar(acc), acc_ph, p.err, kSiteEpilogueFull))) break;
       tc_fence_after_sync();
-      const int n = c.tn * kTN + q * 32 + lane;     // this thread's column of C
+      const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * TM);
+      const int n = c.tn * kTN + nl;   // this thread's column of C
       const bool n_ok = n < p.N;
+      if (w.nseg > 1) {
+        // part of a split tile: publish this partial; the CTA that publishes
+        // last reduces the tile after its work list (see teardown)
+        float* const mine = p.partials +
+                            (static_cast<size_t>(w.tail) * p.max_seg + w.seg) * (TM * kTN) + nl;
 #pragma unroll 1
-      for (int chunk = 0; chunk < TM / 32; ++chunk) {
-        uint32_t v[32];
-        tmem_ld_32cols(tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                           static_cast<uint32_t>(acc * TM + chunk * 32),
-                       v);
-        tmem_wait_ld();
-        const int m0 = c.tm * TM + chunk * 32;
-        if (n_ok) {
-          float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(p.N) + n;
-          const int rows = min(32, p.M - m0);
+        for (int chunk = 0; chunk < TM / 32; ++chunk) {
+          uint32_t v[32];
+          tmem_ld_32cols(t_acc + chunk * 32, v);
+          tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < rows) dst[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * kTN] = __uint_as_float(v[j]);
+        }
+        __threadfence();
+        epilogue_sync();
+        if (nl == 0 && atomicAdd(p.counters + w.tail, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+          // only the first and the last item of a CTA's share can be partial
+          if (*pending_count < kMaxPending)
+            pending[(*pending_count)++] = w;
+          else
+            record_error(p.err, kSitePendingOverflow);
+        }
+      } else {
+#pragma unroll 1
+        for (int chunk = 0; chunk < TM / 32; ++chunk) {
+          uint32_t v[32];
+          tmem_ld_32cols(t_acc + chunk * 32, v);
+          tmem_wait_ld();
+          const int m0 = c.tm * TM + chunk * 32;
+          if (n_ok) {
+            float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(p.N) + n;
+            const int rows = min(32, p.M - m0);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < rows) dst[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+          }
         }
       }
       tc_fence_before_sync();
@@ -317,9 +451,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
-      for (int kt = 0; kt < k_iters; ++kt) {
+    WorkList list(p);
+    while (ok && list.next(p, w)) {
+      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      for (int kt = w.k0; kt < w.k1; ++kt) {
         uint8_t* const st = base_ptr + s * Cfg::STAGE_BYTES;
         // the MMAs of this stage's previous round must be done before its
         // TMEM columns are overwritten (implied on the TMA path, cheap to check)
@@ -404,6 +539,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  // Split tiles whose last partial this CTA published: every thread of the
+  // CTA sums the partials in segment order (fixed, whichever CTA gets here)
+  // and writes C.  Many independent 16-byte loads per thread keep the L2
+  // reads in flight.
+  const int npend = *pending_count;
+  if (npend > 0) {
+    __threadfence();
+    for (int e = 0; e < npend; ++e) {
+      const WorkItem pw = pending[e];
+      const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      const float4* const parts = reinterpret_cast<const float4*>(
+          p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (TM * kTN));
+      constexpr int kVec = TM * kTN / 4;          // float4s per partial
+      constexpr int kPer = kVec / kThreads;       // per thread
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float4 sum[kPer / 2];
+#pragma unroll
+        for (int i = 0; i < kPer / 2; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int sg = 0; sg < pw.nseg; ++sg) {
+          float4 x[kPer / 2];
+#pragma unroll
+          for (int i = 0; i < kPer / 2; ++i)
+            x[i] = __ldcg(parts + static_cast<size_t>(sg) * kVec + threadIdx.x +
+                          (half * (kPer / 2) + i) * kThreads);
+#pragma unroll
+          for (int i = 0; i < kPer / 2; ++i) {
+            sum[i].x += x[i].x;
+            sum[i].y += x[i].y;
+            sum[i].z += x[i].z;
+            sum[i].w += x[i].w;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kPer / 2; ++i) {
+          const int f = threadIdx.x + (half * (kPer / 2) + i) * kThreads;  // float4 index
+          const int m = c.tm * TM + f / (kTN / 4);
+          const int n = c.tn * kTN + (f % (kTN / 4)) * 4;
+          if (m < p.M) {
+            float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n;
+            const float vals[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (n + q < p.N) dst[q] = vals[q];
+          }
+        }
+      }
+      if (threadIdx.x == 0) p.counters[pw.tail] = 0;   // ready for the next call
+    }
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -472,15 +658,17 @@ int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const CUtensorMap& m
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Tile height TM: the one whose persistent schedule gives the busiest SM the
-// least time, counting rounds of tiles x TM / (relative efficiency of that
-// tile height).  Shorter tiles repeat the per-stage transform of B for fewer
-// rows of A and keep the tensor pipe less busy; the efficiencies are the
-// measured 8192^3 throughputs of TM = 128 and 64 relative to TM = 256.
-int choose_tm(const GemmArgs& g) {
+// Tile height TM.  With the split tail the schedule no longer quantises to
+// whole waves, so the most efficient height is used (256; 128 or 64 when M
+// is that small).  Without it (ONE_TILE_PER_CTA or NO_SPLIT_K), the height
+// whose schedule gives the busiest SM the least time: rounds of tiles x TM /
+// (relative efficiency), the efficiencies being the measured 8192^3
+// throughputs of TM = 128 and 64 relative to TM = 256.
+int choose_tm(const GemmArgs& g, bool split_tail) {
   if (g.flags & GEMM_F32_FLAG_TILE64) return 64;
   if (g.flags & GEMM_F32_FLAG_TILE128) return 128;
   if (g.flags & GEMM_F32_FLAG_TILE256) return 256;
+  if (split_tail) return g.M <= 64 ? 64 : (g.M <= 128 ? 128 : 256);
   const long tn = ceil_div(g.N, kTN);
   long best_cost = -1;
   int best = 256;
@@ -498,11 +686,36 @@ int choose_tm(const GemmArgs& g) {
   return best;
 }
 
+// Splits the last partial wave along K.  Fills dp_tiles / sk_ctas / sk_work /
+// max_seg and returns the workspace bytes the split needs (0: no split).
+size_t plan_split_tail(TcParams& p, long tiles, int grid, int tm) {
+  p.dp_tiles = static_cast<int>(tiles);
+  p.sk_ctas = 0;
+  p.sk_work = 0;
+  p.max_seg = 1;
+  const long tail = tiles % grid;
+  if (tail == 0) return 0;
+  const long long work = static_cast<long long>(tail) * p.k_iters;
+  const long long ctas = std::min<long long>(grid, work / kMinSplitIters);
+  if (ctas <= tail) return 0;   // each CTA would still get whole tiles
+  int max_seg = 1;
+  for (long i = 0; i < tail; ++i) {
+    const int first = sk_owner(i * p.k_iters, ctas, work);
+    const int last = sk_owner((i + 1) * static_cast<long long>(p.k_iters) - 1, ctas, work);
+    max_seg = std::max(max_seg, last - first + 1);
+  }
+  if (max_seg == 1 || tail * sizeof(unsigned) > kCounterBytes) return 0;
+  p.dp_tiles = static_cast<int>(tiles - tail);
+  p.sk_ctas = static_cast<int>(ctas);
+  p.sk_work = work;
+  p.max_seg = max_seg;
+  return kCounterBytes + static_cast<size_t>(tail) * max_seg * tm * kTN * sizeof(float);
+}
+
 }  // namespace
 
 int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   *launches = 0;
-  const int tm = choose_tm(g);
   const int bk = nprod == 3 ? 16 : 32;
   TcParams p;
   p.A = g.A;
@@ -511,16 +724,56 @@ int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) 
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
-  p.tiles_m = ceil_div(g.M, tm);
   p.tiles_n = ceil_div(g.N, kTN);
   p.k_iters = ceil_div(g.K, bk);
   p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
+  p.partials = nullptr;
+  p.counters = nullptr;
+  p.sk_ctas = 0;
+  p.sk_work = 0;
+  p.max_seg = 1;
+
+  // Split tail when it applies (with the tallest useful tile); otherwise
+  // whole tiles with the height that best fills the waves.
+  int tm = 0;
+  size_t ws_bytes = 0;
+  if (!(g.flags & (GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K))) {
+    tm = choose_tm(g, true);
+    p.tiles_m = ceil_div(g.M, tm);
+    const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
+    if (tiles <= 0x7fffffffL) ws_bytes = plan_split_tail(p, tiles, g.num_sms, tm);
+  }
+  void* ws = nullptr;
+  int must_clear = 0;
+  if (ws_bytes) ws = acquire_workspace(g.device, stream, ws_bytes, &must_clear);
+  if (!ws) {
+    tm = choose_tm(g, false);
+    p.tiles_m = ceil_div(g.M, tm);
+    p.sk_ctas = 0;
+    p.sk_work = 0;
+    p.max_seg = 1;
+  }
   const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
-  const int grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
-                       ? static_cast<int>(tiles)
-                       : static_cast<int>(std::min<long>(tiles, g.num_sms));
+  int grid;
+  if (ws) {
+    grid = g.num_sms;
+    p.counters = static_cast<unsigned*>(ws);
+    p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+    if (must_clear) {
+      if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return GEMM_F32_ELAUNCH;
+      }
+      *launches += 1;
+    }
+  } else {
+    p.dp_tiles = static_cast<int>(tiles);
+    grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
+               ? static_cast<int>(tiles)
+               : static_cast<int>(std::min<long>(tiles, g.num_sms));
+  }
 
   // TMA needs 16-byte aligned bases and row strides (K % 4 == 0, N % 4 == 0).
   bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && g.K % 4 == 0 && g.N % 4 == 0 &&
@@ -544,7 +797,7 @@ int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) 
     rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
              : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
   }
-  if (rc == GEMM_F32_OK) *launches = 1;
+  if (rc == GEMM_F32_OK) *launches += 1;
   return rc;
 }
 

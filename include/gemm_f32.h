@@ -13,7 +13,15 @@
  *
  * Pointers: caller-owned DEVICE pointers (4-byte aligned), valid on the
  * current device.  The library keeps no reference to them after the call
- * returns and allocates no per-call memory.
+ * returns.
+ *
+ * Workspace: when the output tiles do not fill the last wave of SMs, the
+ * tensor modes split the remaining tiles along K across all SMs; partial
+ * tiles then go through a workspace the library owns, one per (device,
+ * stream).  The first call that needs it (or a larger one) allocates it with
+ * cudaMalloc, which synchronises the device, so make such a call once before
+ * capturing a stream into a CUDA graph; gemm_f32_release() frees it.  Calls
+ * on different streams use different workspaces.
  *
  * Streams: every call is asynchronous on `stream` (0 = legacy default
  * stream) and never synchronises the host, like the stream-taking launcher
@@ -73,6 +81,8 @@ enum gemm_f32_mode {
 #define GEMM_F32_FLAG_TILE256 0x40u      /*   columns); default: chosen by size */
 #define GEMM_F32_FLAG_ONE_TILE_PER_CTA 0x100u /* launch one CTA per output
                                             tile instead of the persistent grid */
+#define GEMM_F32_FLAG_NO_SPLIT_K 0x200u  /* tensor modes: never split the last
+                                            wave along K (no workspace)      */
 #define GEMM_F32_FLAG_TEST_DROP_COPY 0x1000u /* testing only, tensor modes on
                                             the TMA path: CTA 0 never issues
                                             its first operand copy, so its
@@ -101,8 +111,13 @@ int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K,
 int gemm_f32_status(gemm_f32_stream_t stream, unsigned* site);
 
 /* Number of kernels the last successful call on this host thread launched
- * (0 for a no-op, 1 for a GEMM, 1 for the K == 0 memset). */
+ * (0 for a no-op, 1 for a GEMM or for the K == 0 memset, 2 when a split-tail
+ * workspace had to be re-zeroed first). */
 int gemm_f32_last_launches(void);
+
+/* Frees the current device's workspaces after synchronising the device.
+ * Returns 0, or GEMM_F32_EDEVICE / GEMM_F32_ELAUNCH on a CUDA error. */
+int gemm_f32_release(void);
 
 /* Static version string, e.g. "gemm_f32 1.0 sm_103a". */
 const char* gemm_f32_version(void);

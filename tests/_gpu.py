@@ -46,8 +46,8 @@ def run_abi(A: np.ndarray, B: np.ndarray, mode="tc3x", flags=0, offset_a=0, offs
     for _ in range(repeats):
         rc = g.gemm_f32_ex(a_ptr, b_ptr, c_ptr, M, N, K, mode, flags, s)
         assert rc == g.GEMM_F32_OK, "gemm_f32_ex returned %d" % rc
-        expect = 0 if (M == 0 or N == 0) else 1
-        assert g.gemm_f32_last_launches() == expect
+        expect = (0,) if (M == 0 or N == 0) else (1, 2)
+        assert g.gemm_f32_last_launches() in expect
         st, site = g.gemm_f32_status(s)
         assert st == g.GEMM_F32_OK, "device error word: site %d" % site
         host = c_buf.cpu().numpy().view(np.uint32)

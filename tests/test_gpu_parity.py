@@ -18,6 +18,7 @@ MODES = ["tc3x", "ffma", "tc1x"]
 FLAG_STAGED = 0x1
 FLAG_TILE = {64: 0x10, 128: 0x20, 256: 0x40}
 FLAG_ONE_TILE = 0x100
+FLAG_NO_SPLIT = 0x200
 
 
 @pytest.fixture(scope="module")
@@ -167,3 +168,32 @@ def test_large_config_tc1x_sampled():
     rows, cols = sample_indices(A.shape[0], B.shape[1], 2000, 99)
     vals, absv = oracle.gemm_entries(A, B, rows, cols)
     assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc1x"], "c4/tc1x")
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("shape", [(700, 2000, 900), (700, 2001, 900), (256, 4096, 384),
+                                   (512, 16384, 512), (3000, 2048, 2000), (1024, 512, 1024)])
+def test_split_tail_matches_whole_tiles(mode, shape):
+    """Tiles split along K (workspace, fixed-order sum) against whole tiles."""
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "normal", M + K + N)
+    Co, absAB = oracle_full(A, B)
+    C_split, outs = run_abi(A, B, mode, 0, repeats=2)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    C_whole, _ = run_abi(A, B, mode, FLAG_NO_SPLIT)
+    assert_close(C_split, Co, absAB, TOL[mode], "split %s/%s" % (shape, mode))
+    assert_close(C_whole, Co, absAB, TOL[mode], "whole %s/%s" % (shape, mode))
+
+
+def test_split_tail_on_two_streams_and_after_release():
+    import torch
+    from tests._gpu import lib
+    g = lib()
+    A, B = workloads.make_inputs(1001, 513, 777, "uniform", 31)
+    Co, absAB = oracle_full(A, B)
+    s2 = torch.cuda.Stream(torch.device("cuda:0"))
+    C, _ = run_abi(A, B, "tc3x", stream=s2)
+    assert_close(C, Co, absAB, TOL["tc3x"], "second stream")
+    assert g.gemm_f32_release() == g.GEMM_F32_OK
+    C, _ = run_abi(A, B, "tc3x")
+    assert_close(C, Co, absAB, TOL["tc3x"], "after release")
