@@ -19,6 +19,8 @@ GEMM_F32_EINVAL = -1
 GEMM_F32_EDEVICE = -2
 GEMM_F32_ELAUNCH = -3
 GEMM_F32_ETIMEOUT = -4
+GEMM_F32_ESCRATCH = -5
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 MODE_TC3X = 0
 MODE_FFMA = 1
@@ -38,6 +40,7 @@ _ERRORS = {
     GEMM_F32_EDEVICE: "unsupported device (needs sm_103, GB300)",
     GEMM_F32_ELAUNCH: "kernel launch refused by the CUDA runtime",
     GEMM_F32_ETIMEOUT: "a bounded device-side wait ran out",
+    GEMM_F32_ESCRATCH: "the product needs more scratch than the library's fixed array",
 }
 
 
@@ -60,6 +63,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_status.restype = ci
     lib.gemm_f32_last_launches.argtypes = []
     lib.gemm_f32_last_launches.restype = ci
+    lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+    lib.gemm_f32_noalloc.restype = ci
     lib.gemm_f32_release.argtypes = []
     lib.gemm_f32_release.restype = ci
     lib.gemm_f32_version.argtypes = []
@@ -112,6 +117,14 @@ def gemm_f32_ex(A, B, C, M: int, N: int, K: int, mode=MODE_TC3X, flags: int = 0,
     if isinstance(mode, str):
         mode = MODES[mode]
     return lib().gemm_f32_ex(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(mode), int(flags), _stream(stream))
+
+
+def gemm_f32_noalloc(A, B, C, M: int, N: int, K: int, mode=MODE_TC3X, stream=None) -> int:
+    """C = A * B in a tensor mode without any device allocation (scratch from
+    a fixed array inside the library); see include/gemm_f32.h."""
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return lib().gemm_f32_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(mode), _stream(stream))
 
 
 def gemm_f32_status(stream=None):

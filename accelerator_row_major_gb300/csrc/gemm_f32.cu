@@ -194,6 +194,52 @@ extern "C" int gemm_f32(const float* A, const float* B, float* C, int M, int N, 
   return gemm_f32_ex(A, B, C, M, N, K, default_mode(), 0u, stream);
 }
 
+extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
+                                int mode, gemm_f32_stream_t stream_handle) {
+  t_last_launches = 0;
+  if (M < 0 || N < 0 || K < 0) return GEMM_F32_EINVAL;
+  if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_TC1X) return GEMM_F32_EINVAL;
+  if (M == 0 || N == 0) return GEMM_F32_OK;
+  const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+  const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * sizeof(float);
+  const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * sizeof(float);
+  if (C == nullptr) return GEMM_F32_EINVAL;
+  if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_F32_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 3u)
+    return GEMM_F32_EINVAL;
+  if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return GEMM_F32_EINVAL;
+
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  if (K == 0) {
+    if (cudaMemsetAsync(C, 0, c_bytes, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
+    t_last_launches = 1;
+    return GEMM_F32_OK;
+  }
+  gemm_f32_impl::GemmArgs g;
+  g.A = A;
+  g.B = B;
+  g.C = C;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.err = st->err;
+  g.num_sms = st->num_sms;
+  g.device = dev;
+  g.flags = 0;
+  int launches = 0;
+  const int rc = gemm_f32_impl::launch_tc_fixed_scratch(
+      g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream, &launches);
+  if (rc == GEMM_F32_OK) t_last_launches = launches;
+  return rc;
+}
+
 extern "C" int gemm_f32_status(gemm_f32_stream_t stream_handle, unsigned* site) {
   if (site) *site = 0;
   int dev = 0;

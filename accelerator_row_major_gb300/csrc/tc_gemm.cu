@@ -801,4 +801,104 @@ int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) 
   return rc;
 }
 
+// ---------------------------------------------------------------- fixed-scratch variant
+// The split tail's scratch (tile counters and partial tiles) for
+// gemm_f32_noalloc, compiled into the library instead of allocated: every
+// device that loads this module holds these bytes until the process exits.
+// All calls on a device share it, so calls that overlap on the GPU race.
+static __device__ __align__(256) unsigned char g_fixed_scratch[GEMM_F32_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+struct FixedScratch {
+  std::once_flag once;
+  void* ptr = nullptr;   // device address of g_fixed_scratch on this device
+};
+FixedScratch g_fixed[kMaxDevices];
+
+}  // namespace
+
+int launch_tc_fixed_scratch(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+  *launches = 0;
+  if (g.device < 0 || g.device >= kMaxDevices) return GEMM_F32_EDEVICE;
+  // In host code g_fixed_scratch only names the array; its device address is
+  // asked for once per device, with that device current (the caller's).
+  FixedScratch& fs = g_fixed[g.device];
+  std::call_once(fs.once, [&fs] {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_fixed_scratch) == cudaSuccess)
+      fs.ptr = ptr;
+    else
+      (void)cudaGetLastError();
+  });
+  if (!fs.ptr) return GEMM_F32_EDEVICE;
+
+  const int bk = nprod == 3 ? 16 : 32;
+  TcParams p;
+  p.A = g.A;
+  p.B = g.B;
+  p.C = g.C;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles_n = ceil_div(g.N, kTN);
+  p.k_iters = ceil_div(g.K, bk);
+  p.drop_first_copy = 0;
+  p.err = g.err;
+  p.partials = nullptr;
+  p.counters = nullptr;
+  int tm = choose_tm(g, true);
+  p.tiles_m = ceil_div(g.M, tm);
+  long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
+  const size_t need = plan_split_tail(p, tiles, g.num_sms, tm);
+  if (need > GEMM_F32_NOALLOC_SCRATCH_BYTES) return GEMM_F32_ESCRATCH;
+  int grid;
+  if (need) {
+    grid = g.num_sms;
+    p.counters = static_cast<unsigned*>(fs.ptr);
+    p.partials = reinterpret_cast<float*>(static_cast<char*>(fs.ptr) + kCounterBytes);
+    // the counters must start at zero; the array holds whatever the last
+    // call (or a call that gave up on a wait) left there
+    if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
+    *launches += 1;
+  } else {
+    tm = choose_tm(g, false);
+    p.tiles_m = ceil_div(g.M, tm);
+    tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
+    if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
+    p.dp_tiles = static_cast<int>(tiles);
+    p.sk_ctas = 0;
+    p.sk_work = 0;
+    p.max_seg = 1;
+    grid = static_cast<int>(std::min<long>(tiles, g.num_sms));
+  }
+
+  bool tma = g.K % 4 == 0 && g.N % 4 == 0 && reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+  alignas(64) CUtensorMap ma, mb;
+  if (tma) {
+    tma = encode_2d(&ma, g.A, g.M, g.K, bk, tm,
+                    bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
+          encode_2d(&mb, g.B, g.K, g.N, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!tma) {
+    memset(&ma, 0, sizeof(ma));
+    memset(&mb, 0, sizeof(mb));
+  }
+  int rc;
+  if (nprod == 3) {
+    rc = tma ? launch_tm<16, 3, true>(tm, g, p, ma, mb, grid, stream)
+             : launch_tm<16, 3, false>(tm, g, p, ma, mb, grid, stream);
+  } else {
+    rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
+             : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
+  }
+  if (rc == GEMM_F32_OK) *launches += 1;
+  return rc;
+}
+
 }  // namespace gemm_f32_impl

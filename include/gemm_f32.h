@@ -53,8 +53,12 @@ enum gemm_f32_status_code {
                                CUDA query failed                           */
     GEMM_F32_ELAUNCH = -3,  /* the kernel launch (or the K == 0 memset) was
                                refused by the CUDA runtime                  */
-    GEMM_F32_ETIMEOUT = -4  /* gemm_f32_status(): a bounded device-side wait
+    GEMM_F32_ETIMEOUT = -4, /* gemm_f32_status(): a bounded device-side wait
                                ran out; C of that call is undefined         */
+    GEMM_F32_ESCRATCH = -5  /* gemm_f32_noalloc(): the product would need
+                               more scratch than the library's fixed array
+                               (GEMM_F32_NOALLOC_SCRATCH_BYTES); nothing was
+                               launched                                     */
 };
 
 /* Arithmetic modes of gemm_f32_ex. */
@@ -118,6 +122,34 @@ int gemm_f32_last_launches(void);
 /* Frees the current device's workspaces after synchronising the device.
  * Returns 0, or GEMM_F32_EDEVICE / GEMM_F32_ELAUNCH on a CUDA error. */
 int gemm_f32_release(void);
+
+/* Size of the scratch array compiled into the library for gemm_f32_noalloc
+ * (32 MiB, held on every device that loads the library until exit). */
+#define GEMM_F32_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* C = A * B in a tensor mode (GEMM_F32_MODE_TC3X or GEMM_F32_MODE_TC1X)
+ * without allocating any device memory.  The pages have no counterpart: it
+ * exists for callers that must not allocate -- code that runs where
+ * cudaMalloc is not allowed or not safe, such as a host that has handed all
+ * device memory to its own pool, a latency-critical path that cannot take
+ * cudaMalloc's implicit device synchronisation, or an embedding that must
+ * keep the library's memory footprint fixed after start-up.  gemm_f32_ex may
+ * allocate its split-tail workspace on first use; this call takes that
+ * scratch from a fixed array inside the library instead and never calls
+ * cudaMalloc, cudaFree or any allocating routine.
+ *   - The caller still passes A, B and C (device pointers, as gemm_f32).
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up); make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps what the
+ *     last call left in it: two such calls whose kernels overlap on the GPU
+ *     (for example on two streams) race and give wrong results.  Each call
+ *     re-zeroes the part of the array that must start at zero.
+ *   - Returns GEMM_F32_ESCRATCH, launching nothing, when the product's
+ *     split tail would need more than GEMM_F32_NOALLOC_SCRATCH_BYTES; other
+ *     errors as gemm_f32_ex (GEMM_F32_EINVAL for mode FFMA or a bad mode).
+ * The result equals gemm_f32_ex's for the same mode. */
+int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
+                     int mode, gemm_f32_stream_t stream);
 
 /* Static version string, e.g. "gemm_f32 1.0 sm_103a". */
 const char* gemm_f32_version(void);

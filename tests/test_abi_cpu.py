@@ -22,7 +22,8 @@ def g():
 def test_header_declares_the_entry_points(g):
     names = g.declared_symbols()
     assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status",
-                            "gemm_f32_last_launches", "gemm_f32_release", "gemm_f32_version"])
+                            "gemm_f32_last_launches", "gemm_f32_noalloc", "gemm_f32_release",
+                            "gemm_f32_version"])
 
 
 def test_library_exports_every_declared_symbol(g):

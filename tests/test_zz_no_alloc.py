@@ -1,0 +1,94 @@
+"""gemm_f32_noalloc: the tensor-core product with its scratch taken from a
+fixed array inside the library, for callers that must not allocate device
+memory (a host whose memory all belongs to its own pool, a path that cannot
+take cudaMalloc's implicit synchronisation, a fixed footprint after start-up).
+
+Kept in a file that pytest collects last, so that a stop at the first failure
+has already run every other test.  It passes alone in a fresh process and
+after the other tests: the first library call made here loads the module.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from tests._gpu import GUARD, SENTINEL, TOL, assert_close, lib, oracle_full
+
+pytestmark = pytest.mark.gpu
+
+
+def _guarded(shape, dev):
+    import torch
+    host = np.full(GUARD + shape[0] * shape[1] + GUARD, SENTINEL, dtype=np.uint32)
+    return torch.from_numpy(host.view(np.float32)).to(dev)
+
+
+def _inner(buf, shape):
+    host = buf.cpu().numpy().view(np.uint32)
+    n = shape[0] * shape[1]
+    guards_ok = bool(np.all(host[:GUARD] == SENTINEL) and np.all(host[GUARD + n:] == SENTINEL))
+    return host[GUARD:GUARD + n].view(np.float32).reshape(shape).copy(), guards_ok
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+def test_noalloc_matches_gemm_f32_ex_twice_in_a_row(mode):
+    import torch
+
+    g = lib()
+    # 3000 x 4096 x 2000 splits its last partial wave along K in both modes,
+    # so the fixed scratch array is used (about 26 / 15 MiB of it)
+    M, K, N = 3000, 4096, 2000
+    A, B = workloads.make_inputs(M, K, N, "normal", 77)
+    Co, absAB = oracle_full(A, B)
+    dev = torch.device("cuda:0")
+    s = torch.cuda.current_stream(dev)
+    At = torch.from_numpy(A).to(dev)
+    Bt = torch.from_numpy(B).to(dev)
+    ref_buf = _guarded((M, N), dev)
+    out_bufs = [_guarded((M, N), dev), _guarded((M, N), dev)]
+
+    # the existing entry point first: loads the module and its own workspace
+    ptr = lambda b: b.data_ptr() + 4 * GUARD  # noqa: E731
+    assert g.gemm_f32_ex(At, Bt, ptr(ref_buf), M, N, K, mode, 0, s) == g.GEMM_F32_OK
+    assert g.gemm_f32_status(s) == (g.GEMM_F32_OK, 0)
+    C_ref, ok = _inner(ref_buf, (M, N))
+    assert ok
+    assert_close(C_ref, Co, absAB, TOL[mode], "gemm_f32_ex/%s" % mode)
+
+    torch.cuda.synchronize(dev)
+    free_before = torch.cuda.mem_get_info(dev)[0]
+    for call, buf in enumerate(out_bufs):
+        rc = g.gemm_f32_noalloc(At, Bt, ptr(buf), M, N, K, mode, s)
+        assert rc == g.GEMM_F32_OK, "gemm_f32_noalloc returned %d" % rc
+        assert g.gemm_f32_last_launches() == 2          # counter reset + the GEMM
+        assert g.gemm_f32_status(s) == (g.GEMM_F32_OK, 0)
+        C, ok = _inner(buf, (M, N))
+        assert ok, "call %d wrote outside C" % call
+        assert_close(C, C_ref, absAB, TOL[mode], "noalloc call %d vs gemm_f32_ex/%s" % (call, mode))
+        assert_close(C, Co, absAB, TOL[mode], "noalloc call %d vs oracle/%s" % (call, mode))
+    torch.cuda.synchronize(dev)
+    assert torch.cuda.mem_get_info(dev)[0] == free_before, "device memory changed"
+
+
+def test_noalloc_rejects_products_beyond_its_scratch():
+    import torch
+
+    g = lib()
+    # 2048^3 in tc3x: 128 tiles, each shared by two CTAs -> 32 MiB of partial
+    # tiles plus the counters, just over the fixed array
+    M = N = K = 2048
+    dev = torch.device("cuda:0")
+    At = torch.zeros((M, K), dtype=torch.float32, device=dev)
+    Bt = torch.zeros((K, N), dtype=torch.float32, device=dev)
+    buf = _guarded((M, N), dev)
+    rc = g.gemm_f32_noalloc(At, Bt, buf.data_ptr() + 4 * GUARD, M, N, K, "tc3x",
+                            torch.cuda.current_stream(dev))
+    assert rc == g.GEMM_F32_ESCRATCH
+    assert g.gemm_f32_last_launches() == 0
+    _, ok = _inner(buf, (M, N))
+    C, _ = _inner(buf, (M, N))
+    assert ok and np.all(C.view(np.uint32) == SENTINEL), "nothing may be written"
+
+
+def test_noalloc_rejects_the_ffma_mode():
+    g = lib()
+    assert g.gemm_f32_noalloc(0x1000, 0x2000, 0x3000, 4, 4, 4, "ffma") == g.GEMM_F32_EINVAL
