@@ -50,8 +50,8 @@ MODE_PRODUCTS = {"tc3x": 3, "tc1x": 1, "ffma": 1}
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c5a", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--mode", default="tc3x", choices=sorted(MODE_PRODUCTS))
@@ -113,7 +113,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms while active."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms while active."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -128,7 +128,7 @@ class ClockSampler:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                     "--format=csv,noheader,nounits", "-lms", "100"],
+                     "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
