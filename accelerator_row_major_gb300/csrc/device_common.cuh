@@ -3,6 +3,8 @@
 // hanging, and thin inline-PTX wrappers for mbarrier, TMA and tcgen05.
 #pragma once
 
+#include <algorithm>
+#include <cstddef>
 #include <cstdint>
 
 namespace gemm_f32_dev {
@@ -53,6 +55,155 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n,
   c.tm = first_m + r % rows_here;
   c.tn = r / rows_here;
   return c;
+}
+
+// ---------------------------------------------------------------- split tail
+// When the output tiles do not fill the last wave of CTAs, the remaining
+// ("tail") tiles' K iterations are shared evenly by the CTAs.  Work list of
+// CTA c (grid G): whole tiles c, c+G, ... below dp_tiles, then iterations
+// [start(c), start(c+1)) of the tail's flattened (tile, K iteration) space.
+// A CTA that computes only part of a tile writes it to a workspace slot and
+// bumps the tile's counter; the CTA that bumps it last adds the partials in
+// segment order (fixed: the sum does not depend on which CTA is last).
+constexpr int kMinSplitIters = 64;       // least K iterations per CTA in the split tail
+constexpr size_t kCounterBytes = 4096;   // tile counters at the start of the workspace
+
+// One unit of a CTA's work: K iterations [k0, k1) of one output tile.
+struct WorkItem {
+  int tile, k0, k1;
+  int tail;        // index among the split tiles, or -1 for a whole tile
+  int seg, nseg;   // this CTA's position among the CTAs sharing the tile
+};
+
+__host__ __device__ __forceinline__ long long sk_start(long long c, long long ctas, long long work) {
+  return c * work / ctas;
+}
+// CTA whose share of the split K iterations contains iteration x
+__host__ __device__ __forceinline__ int sk_owner(long long x, long long ctas, long long work) {
+  return static_cast<int>(((x + 1) * ctas - 1) / work);
+}
+
+// The work list of one CTA, walked identically by every role.  P provides
+// k_iters, dp_tiles, sk_ctas and sk_work.
+struct WorkList {
+  int next_dp;
+  long long x, x_end;
+
+  template <class P>
+  __device__ __forceinline__ explicit WorkList(const P& p) {
+    next_dp = blockIdx.x;
+    x = x_end = 0;
+    if (static_cast<int>(blockIdx.x) < p.sk_ctas) {
+      x = sk_start(blockIdx.x, p.sk_ctas, p.sk_work);
+      x_end = sk_start(blockIdx.x + 1, p.sk_ctas, p.sk_work);
+    }
+  }
+
+  template <class P>
+  __device__ __forceinline__ bool next(const P& p, WorkItem& w) {
+    if (next_dp < p.dp_tiles) {
+      w.tile = next_dp;
+      w.k0 = 0;
+      w.k1 = p.k_iters;
+      w.tail = -1;
+      w.seg = 0;
+      w.nseg = 1;
+      next_dp += gridDim.x;
+      return true;
+    }
+    if (x < x_end) {
+      const long long ki = p.k_iters;
+      const int i = static_cast<int>(x / ki);
+      w.tile = p.dp_tiles + i;
+      w.tail = i;
+      w.k0 = static_cast<int>(x - i * ki);
+      w.k1 = static_cast<int>(min(ki, w.k0 + (x_end - x)));
+      const int first = sk_owner(i * ki, p.sk_ctas, p.sk_work);
+      const int last = sk_owner((i + 1) * ki - 1, p.sk_ctas, p.sk_work);
+      w.seg = static_cast<int>(blockIdx.x) - first;
+      w.nseg = last - first + 1;
+      x += w.k1 - w.k0;
+      return true;
+    }
+    return false;
+  }
+};
+
+// Host: splits the last partial wave along K.  Fills p.dp_tiles / sk_ctas /
+// sk_work / max_seg (p.k_iters must be set) and returns the workspace bytes
+// the split needs, 0 when whole tiles are better (no split).
+template <class P>
+inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_bytes) {
+  p.dp_tiles = static_cast<int>(tiles);
+  p.sk_ctas = 0;
+  p.sk_work = 0;
+  p.max_seg = 1;
+  const long tail = tiles % grid;
+  if (tail == 0) return 0;
+  const long long work = static_cast<long long>(tail) * p.k_iters;
+  const long long ctas = std::min<long long>(grid, work / kMinSplitIters);
+  if (ctas <= tail) return 0;   // each CTA would still get whole tiles
+  int max_seg = 1;
+  for (long i = 0; i < tail; ++i) {
+    const int first = sk_owner(i * p.k_iters, ctas, work);
+    const int last = sk_owner((i + 1) * static_cast<long long>(p.k_iters) - 1, ctas, work);
+    max_seg = std::max(max_seg, last - first + 1);
+  }
+  if (max_seg == 1 || tail * sizeof(unsigned) > kCounterBytes) return 0;
+  p.dp_tiles = static_cast<int>(tiles - tail);
+  p.sk_ctas = static_cast<int>(ctas);
+  p.sk_work = work;
+  p.max_seg = max_seg;
+  return kCounterBytes + static_cast<size_t>(tail) * max_seg * partial_tile_bytes;
+}
+
+// Device: every thread of the CTA (NTHREADS) adds the nseg partial tiles at
+// `parts` ([seg][ROWS][COLS] fp32) in segment order and writes the sum to C
+// rows m0.., columns n0.. (masked).  CHUNK independent 16-byte loads per
+// thread per partial keep the L2 reads in flight; a kernel whose hot loops
+// need few registers takes a small CHUNK so that this end-of-work code does
+// not set its register count.
+template <int ROWS, int COLS, int NTHREADS, int CHUNK>
+__device__ __forceinline__ void reduce_partials(const float* parts, int nseg, int m0, int n0,
+                                                int M, int N, float* C) {
+  constexpr int kVec = ROWS * COLS / 4;            // float4s per partial
+  constexpr int kPer = kVec / NTHREADS;            // per thread
+  constexpr int kChunk = kPer < CHUNK ? kPer : CHUNK;
+  static_assert(kVec % NTHREADS == 0 && kPer % kChunk == 0, "partial tile shape");
+  const float4* const p4 = reinterpret_cast<const float4*>(parts);
+#pragma unroll 1
+  for (int base = 0; base < kPer; base += kChunk) {
+    float4 sum[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int sg = 0; sg < nseg; ++sg) {
+      float4 x[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+        x[i] = __ldcg(p4 + static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        sum[i].x += x[i].x;
+        sum[i].y += x[i].y;
+        sum[i].z += x[i].z;
+        sum[i].w += x[i].w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int f = threadIdx.x + (base + i) * NTHREADS;   // float4 index in the tile
+      const int m = m0 + f / (COLS / 4);
+      const int n = n0 + (f % (COLS / 4)) * 4;
+      if (m < M) {
+        float* dst = C + static_cast<size_t>(m) * static_cast<size_t>(N) + n;
+        const float v[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (n + q < N) dst[q] = v[q];
+      }
+    }
+  }
 }
 
 // ---------------------------------------------------------------- shared memory

@@ -1,20 +1,32 @@
-// CUDA-core FP32 GEMM (FFMA) for sm_103a: persistent CTAs, 128 x 128 output
-// tiles, 8 x 8 outputs per thread, double-buffered shared memory.
+// CUDA-core FP32 GEMM (FFMA) for sm_103a: persistent CTAs, 128 x 256 output
+// tiles, 8 x 16 outputs per thread, a 4-stage cp.async shared-memory ring,
+// and the paired fp32 fused multiply-add (fma.rn.f32x2: two FMAs per lane
+// per instruction, each rounded once like fmaf).
 //
 // Computes C[i][j] = sum_k A[i][k] * B[k][j] (row-major) in fp32 fused
 // multiply-adds, k ascending per output.  The structure follows the pages'
-// last step -- 2-D register coarsening, where each thread keeps a small tile
-// of C in registers and reuses every loaded A and B value across it
-// ("LeetGPU problem 2: matrix multiplication", yekq.top, section v4) -- on
-// top of shared-memory K tiles ("Lesson 10: shared-memory tiled GEMM",
-// hpc.payai.win, section 2).  Differences: one barrier per K tile instead of
-// two (the tile being written is never the one being read), 16-byte loads
-// where the strides allow, and a persistent grid.  Out-of-range elements
-// load as 0 and are never stored; no thread leaves before the last barrier
-// ("Lesson 10", section 3).
+// last step -- 2-D register coarsening, where each thread keeps a tile of C
+// in registers and reuses every loaded A and B value across it ("LeetGPU
+// problem 2: matrix multiplication", yekq.top, section v4) -- on top of
+// shared-memory K tiles ("Lesson 10: shared-memory tiled GEMM",
+// hpc.payai.win, section 2).  Differences: the K tiles are copied by
+// cp.async several tiles ahead (no register staging), one barrier per K
+// tile instead of two (the stage being filled is never the one being read),
+// 16-byte copies where the strides allow, and a persistent grid.
+// Out-of-range elements are zero-filled by the copy and never stored; no
+// thread leaves before the last barrier ("Lesson 10", section 3).
+//
+// The last partial wave is split along K like the tensor-core path's (see
+// device_common.cuh): partial tiles go through the library's workspace.
+//
+// Thread (tx, ty) of the 16 x 16 grid owns rows ty + 16 i (i < 8) and
+// columns 64 g + 4 tx .. +3 (g < 4).  A warp covers 4 values of ty and 8 of
+// tx, so per K step its 16-byte A reads hit 4 consecutive rows (distinct
+// banks with the 20-float row pitch) and its B reads one 128-byte segment.
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "../../include/gemm_f32.h"
@@ -26,136 +38,277 @@ using namespace gemm_f32_dev;
 
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kBK = 8;
+constexpr int kBM = 128, kBN = 256, kBK = 16;
+constexpr int kStages = 4;
 constexpr int kThreads = 256;
-constexpr int kAPitch = kBM + 4;   // padded rows of the transposed A tile
+constexpr int kAPitch = kBK + 4;               // floats per A row in shared memory
+constexpr int kAStage = kBM * kAPitch;         // floats
+constexpr int kBStage = kBK * kBN;             // floats
+constexpr int kSmemBytes = kStages * (kAStage + kBStage) * 4;
 constexpr int kRasterGroup = 8;
-constexpr int kBlocksPerSm = 2;
+constexpr int kMaxPending = 8;               // split tiles one CTA may have to reduce
 
 struct FfmaParams {
   const float* __restrict__ A;
   const float* __restrict__ B;
   float* __restrict__ C;
   int M, N, K;
-  int tiles_m, tiles_n;
+  int tiles_m, tiles_n, k_iters;
+  int dp_tiles;          // tiles 0 .. dp_tiles-1 are computed whole, round robin
+  int sk_ctas;           // CTAs 0 .. sk_ctas-1 share the K iterations of the rest
+  long long sk_work;     // (tiles - dp_tiles) * k_iters
+  int max_seg;           // most CTAs sharing one tail tile
+  float* partials;       // [tail tile][max_seg][128][256] fp32
+  unsigned* counters;    // [tail tile]: partials written so far (zero between calls)
+  unsigned* err;
 };
 
-// VEC: A, B and C rows are 16-byte aligned (K % 4 == 0, N % 4 == 0 and
-// 16-byte aligned bases), so whole float4s are either in or out of range.
+// Two fused multiply-adds per lane: d.x = a.x * b.x + c.x, d.y = a.y * b.y + c.y
+// (each rounded once, as fmaf), on 64-bit register pairs.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint64_t pair(float x, float y) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
+  return d;
+}
+
+__device__ __forceinline__ float2 unpair(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Copies K tile `kt` of the block's A panel and B panel into one stage.
+// VEC: K % 4 == 0, N % 4 == 0 and 16-byte aligned A and B, so a 16-byte
+// chunk is either wholly inside the matrix or wholly outside.
 template <bool VEC>
-__device__ __forceinline__ void load_tile(const FfmaParams& p, int m0, int n0, int k0, float (&ra)[4],
-                                          float (&rb)[4]) {
+__device__ __forceinline__ void load_stage(const FfmaParams& p, int m0, int n0, int kt,
+                                           uint32_t a_dst, uint32_t b_dst) {
   const int tid = threadIdx.x;
-  // A: 128 rows x 8 k; thread -> row tid/2, k (tid%2)*4 .. +3
-  {
-    const int r = m0 + (tid >> 1);
-    const int k = k0 + (tid & 1) * 4;
-    const float* src = p.A + static_cast<size_t>(r) * p.K + k;
+  const int k0 = kt * kBK;
+  // A: 128 rows x 16 k = 512 chunks of 4 floats; thread -> chunks tid, tid + 256
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int c = tid + h * kThreads;
+    const int r = c >> 2, kc = (c & 3) * 4;
+    const int gm = m0 + r, gk = k0 + kc;
+    const uint32_t dst = a_dst + (r * kAPitch + kc) * 4;
     if (VEC) {
-      if (r < p.M && k < p.K) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        ra[0] = v.x; ra[1] = v.y; ra[2] = v.z; ra[3] = v.w;
-      } else {
-        ra[0] = ra[1] = ra[2] = ra[3] = 0.f;
-      }
+      const bool in = gm < p.M && gk < p.K;
+      const float* src = in ? p.A + static_cast<size_t>(gm) * p.K + gk : p.A;
+      cp_async_16(dst, src, in ? 16u : 0u);
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ra[j] = (r < p.M && k + j < p.K) ? __ldg(src + j) : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const bool in = gm < p.M && gk + e < p.K;
+        const float* src = in ? p.A + static_cast<size_t>(gm) * p.K + gk + e : p.A;
+        cp_async_4(dst + 4 * e, src, in ? 4u : 0u);
+      }
     }
   }
-  // B: 8 k x 128 columns; thread -> k tid/32, columns (tid%32)*4 .. +3
-  {
-    const int k = k0 + (tid >> 5);
-    const int n = n0 + (tid & 31) * 4;
-    const float* src = p.B + static_cast<size_t>(k) * p.N + n;
+  // B: 16 k x 256 columns = 1024 chunks; thread -> chunks tid + 256 h
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const int c = tid + h * kThreads;
+    const int k = c >> 6, nc = (c & 63) * 4;
+    const int gk = k0 + k, gn = n0 + nc;
+    const uint32_t dst = b_dst + (k * kBN + nc) * 4;
     if (VEC) {
-      if (k < p.K && n < p.N) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src));
-        rb[0] = v.x; rb[1] = v.y; rb[2] = v.z; rb[3] = v.w;
-      } else {
-        rb[0] = rb[1] = rb[2] = rb[3] = 0.f;
-      }
+      const bool in = gk < p.K && gn < p.N;
+      const float* src = in ? p.B + static_cast<size_t>(gk) * p.N + gn : p.B;
+      cp_async_16(dst, src, in ? 16u : 0u);
     } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) rb[j] = (k < p.K && n + j < p.N) ? __ldg(src + j) : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const bool in = gk < p.K && gn + e < p.N;
+        const float* src = in ? p.B + static_cast<size_t>(gk) * p.N + gn + e : p.B;
+        cp_async_4(dst + 4 * e, src, in ? 4u : 0u);
+      }
     }
   }
 }
 
-__device__ __forceinline__ void store_tile(float (*As)[kAPitch], float (*Bs)[kBN], const float (&ra)[4],
-                                           const float (&rb)[4]) {
-  const int tid = threadIdx.x;
-  const int ar = tid >> 1, ak = (tid & 1) * 4;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) As[ak + j][ar] = ra[j];   // transposed: k-major rows of A
-  *reinterpret_cast<float4*>(&Bs[tid >> 5][(tid & 31) * 4]) = make_float4(rb[0], rb[1], rb[2], rb[3]);
-}
-
 template <bool VEC>
-__global__ void __launch_bounds__(kThreads, kBlocksPerSm) ffma_gemm_kernel(const FfmaParams p) {
-  __shared__ __align__(16) float As[2][kBK][kAPitch];
-  __shared__ __align__(16) float Bs[2][kBK][kBN];
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;   // 16 x 16 threads; thread rows ty*4, 64+ty*4
-  const int num_tiles = p.tiles_m * p.tiles_n;
-  const int k_iters = (p.K + kBK - 1) / kBK;
+__global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams p) {
+  extern __shared__ __align__(16) float smem_f[];
+  __shared__ WorkItem pending[kMaxPending];   // split tiles this CTA must reduce
+  __shared__ int pending_count;
+  float* const As = smem_f;                          // [stage][128][kAPitch]
+  float* const Bs = smem_f + kStages * kAStage;      // [stage][16][256]
+  const uint32_t as_addr = smem_addr(As), bs_addr = smem_addr(Bs);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tx = (warp & 1) * 8 + (lane & 7);
+  const int ty = (warp >> 1) * 4 + (lane >> 3);
+  if (threadIdx.x == 0) pending_count = 0;
 
-  for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-    const TileCoord c = tile_coord(t, p.tiles_m, p.tiles_n, kRasterGroup);
+  WorkList list(p);
+  WorkItem w;
+  while (list.next(p, w)) {
+    const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
     const int m0 = c.tm * kBM, n0 = c.tn * kBN;
-    float acc[8][8];
+    const int nk = w.k1 - w.k0;
+    // acc[i][q] holds C columns 2q, 2q+1 of row i of this thread's 8 x 16
+    uint64_t acc[8][8];
 #pragma unroll
     for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+      for (int q = 0; q < 8; ++q) acc[i][q] = 0ull;
 
-    float ra[4], rb[4];
-    load_tile<VEC>(p, m0, n0, 0, ra, rb);
-    store_tile(As[0], Bs[0], ra, rb);
-    __syncthreads();
-
-    for (int kt = 0; kt < k_iters; ++kt) {
-      const int cur = kt & 1;
-      const bool more = kt + 1 < k_iters;
-      if (more) load_tile<VEC>(p, m0, n0, (kt + 1) * kBK, ra, rb);
+    // prologue: the first kStages-1 tiles in flight (empty groups keep the count)
 #pragma unroll
-      for (int k = 0; k < kBK; ++k) {
-        const float4 a0 = *reinterpret_cast<const float4*>(&As[cur][k][ty * 4]);
-        const float4 a1 = *reinterpret_cast<const float4*>(&As[cur][k][64 + ty * 4]);
-        const float4 b0 = *reinterpret_cast<const float4*>(&Bs[cur][k][tx * 4]);
-        const float4 b1 = *reinterpret_cast<const float4*>(&Bs[cur][k][64 + tx * 4]);
-        const float a[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = __fmaf_rn(a[i], b[j], acc[i][j]);
-      }
-      if (more) store_tile(As[cur ^ 1], Bs[cur ^ 1], ra, rb);
-      __syncthreads();
+    for (int s = 0; s < kStages - 1; ++s) {
+      if (s < nk)
+        load_stage<VEC>(p, m0, n0, w.k0 + s, as_addr + s * kAStage * 4, bs_addr + s * kBStage * 4);
+      cp_async_commit();
     }
 
-    // epilogue: rows ty*4+i and 64+ty*4+i, columns tx*4.. and 64+tx*4..
-    const bool c_vec = VEC;
+    for (int j = 0; j < nk; ++j) {
+      cp_async_wait<kStages - 2>();   // this thread's copies of tile j have landed
+      __syncthreads();                // everyone's have; stage (j-1) % S is free
+      const int nxt = j + kStages - 1;
+      if (nxt < nk) {
+        const int s = nxt % kStages;
+        load_stage<VEC>(p, m0, n0, w.k0 + nxt, as_addr + s * kAStage * 4,
+                        bs_addr + s * kBStage * 4);
+      }
+      cp_async_commit();
+
+      const float* const as = As + (j % kStages) * kAStage;
+      const float* const bs = Bs + (j % kStages) * kBStage;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + (i - 4));
-      if (r >= p.M) continue;
-      float* crow = p.C + static_cast<size_t>(r) * p.N;
+      for (int kg = 0; kg < kBK / 4; ++kg) {
+        float4 a4[8];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int n = n0 + h * 64 + tx * 4;
-        if (c_vec && n + 3 < p.N) {
-          *reinterpret_cast<float4*>(crow + n) =
-              make_float4(acc[i][h * 4], acc[i][h * 4 + 1], acc[i][h * 4 + 2], acc[i][h * 4 + 3]);
-        } else {
+        for (int i = 0; i < 8; ++i)
+          a4[i] = *reinterpret_cast<const float4*>(as + (ty + 16 * i) * kAPitch + kg * 4);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (n + j < p.N) crow[n + j] = acc[i][h * 4 + j];
+        for (int kk = 0; kk < 4; ++kk) {
+          uint64_t b[8];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const ulonglong2 v =
+                *reinterpret_cast<const ulonglong2*>(bs + (kg * 4 + kk) * kBN + g * 64 + tx * 4);
+            b[2 * g] = v.x;
+            b[2 * g + 1] = v.y;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+            const uint64_t aa = pair(a, a);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[i][q] = fma2(aa, b[q], acc[i][q]);
+          }
         }
       }
     }
+    cp_async_wait<0>();
+    __syncthreads();   // the next item's prologue overwrites stages still being read
+
+    if (w.nseg == 1) {
+      // epilogue: rows ty + 16 i, columns 64 g + 4 tx .. +3
+      const bool c_vec = VEC && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = m0 + ty + 16 * i;
+        if (r >= p.M) continue;
+        float* crow = p.C + static_cast<size_t>(r) * p.N;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int n = n0 + g * 64 + tx * 4;
+          const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
+          const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+          if (c_vec && n + 3 < p.N) {
+            *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (n + q < p.N) crow[n + q] = v[q];
+          }
+        }
+      }
+    } else {
+      // part of a split tile: publish it; the CTA that publishes last reduces
+      // the tile after its work list
+      float* const slot =
+          p.partials + (static_cast<size_t>(w.tail) * p.max_seg + w.seg) * (kBM * kBN);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
+          *reinterpret_cast<float4*>(slot + (ty + 16 * i) * kBN + g * 64 + tx * 4) =
+              make_float4(lo.x, lo.y, hi.x, hi.y);
+        }
+      }
+      __threadfence();
+      __syncthreads();
+      if (threadIdx.x == 0 &&
+          atomicAdd(p.counters + w.tail, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+        // only the first and the last item of a CTA's share can be partial
+        if (pending_count < kMaxPending)
+          pending[pending_count++] = w;
+        else
+          record_error(p.err, kSitePendingOverflow);
+      }
+    }
   }
+
+  __syncthreads();
+  const int npend = pending_count;
+  if (npend > 0) {
+    __threadfence();
+    for (int e = 0; e < npend; ++e) {
+      const WorkItem pw = pending[e];
+      const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      reduce_partials<kBM, kBN, kThreads, 8>(
+          p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (kBM * kBN), pw.nseg,
+          c.tm * kBM, c.tn * kBN, p.M, p.N, p.C);
+      if (threadIdx.x == 0) p.counters[pw.tail] = 0;   // ready for the next call
+    }
+  }
+}
+
+constexpr int kMaxDevices = 64;
+
+template <bool VEC>
+int launch_vec(const GemmArgs& g, const FfmaParams& p, int grid, cudaStream_t stream) {
+  static std::atomic<unsigned long long> configured{0};  // bit per device
+  const unsigned long long bit = 1ull << (g.device % kMaxDevices);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(ffma_gemm_kernel<VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
+    configured.fetch_or(bit);
+  }
+  ffma_gemm_kernel<VEC><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  return GEMM_F32_OK;
 }
 
 }  // namespace
@@ -171,21 +324,43 @@ int launch_ffma(const GemmArgs& g, cudaStream_t stream, int* launches) {
   p.K = g.K;
   p.tiles_m = (g.M + kBM - 1) / kBM;
   p.tiles_n = (g.N + kBN - 1) / kBN;
+  p.k_iters = (g.K + kBK - 1) / kBK;
+  p.partials = nullptr;
+  p.counters = nullptr;
+  p.err = g.err;
   const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
+  p.dp_tiles = static_cast<int>(tiles);
+  p.sk_ctas = 0;
+  p.sk_work = 0;
+  p.max_seg = 1;
+  int grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
+                 ? static_cast<int>(tiles)
+                 : static_cast<int>(std::min<long>(tiles, g.num_sms));
+  if (!(g.flags & (GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K))) {
+    FfmaParams q = p;
+    const size_t ws_bytes = plan_split_tail(q, tiles, g.num_sms, sizeof(float) * kBM * kBN);
+    int must_clear = 0;
+    void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes, &must_clear) : nullptr;
+    if (ws) {
+      p = q;
+      grid = g.num_sms;
+      p.counters = static_cast<unsigned*>(ws);
+      p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+      if (must_clear) {
+        if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
+          (void)cudaGetLastError();
+          return GEMM_F32_ELAUNCH;
+        }
+        *launches += 1;
+      }
+    }
+  }
   const bool vec = g.K % 4 == 0 && g.N % 4 == 0 && reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(g.B) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(g.C) % 16 == 0;
-  const int grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
-                       ? static_cast<int>(tiles)
-                       : static_cast<int>(std::min<long>(tiles, static_cast<long>(g.num_sms) * kBlocksPerSm));
-  if (vec)
-    ffma_gemm_kernel<true><<<grid, kThreads, 0, stream>>>(p);
-  else
-    ffma_gemm_kernel<false><<<grid, kThreads, 0, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
-  *launches = 1;
-  return GEMM_F32_OK;
+                   reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+  const int rc = vec ? launch_vec<true>(g, p, grid, stream) : launch_vec<false>(g, p, grid, stream);
+  if (rc == GEMM_F32_OK) *launches += 1;
+  return rc;
 }
 
 }  // namespace gemm_f32_impl

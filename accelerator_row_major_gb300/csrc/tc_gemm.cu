@@ -74,13 +74,7 @@ constexpr int kEpilogueBarrier = 1;          // named barrier of the epilogue wa
 constexpr int kSmemLimit = 232448;           // opt-in dynamic shared memory per block
 constexpr int kTmemCols = 512;
 constexpr int kRasterGroup = 8;              // tile-rows per L2 group
-constexpr int kMinSplitIters = 64;           // least K iterations per CTA in the split tail
 constexpr int kMaxPending = 8;               // split tiles one CTA may have to reduce
-// Split-tail counters live at the start of the workspace, one per tail tile
-// (a tail has fewer tiles than there are SMs), at the same place for every
-// problem, so the zeros the last CTA of each tile leaves behind are seen by
-// the next call whatever its shape.
-constexpr size_t kCounterBytes = 4096;
 
 struct TcParams {
   const float* A;
@@ -96,64 +90,6 @@ struct TcParams {
   unsigned* counters;    // [tail tile]: partials written so far (zero between calls)
   int drop_first_copy;   // testing only: CTA 0 skips its first copy
   unsigned* err;
-};
-
-// One unit of a CTA's work: K iterations [k0, k1) of one output tile.
-struct WorkItem {
-  int tile, k0, k1;
-  int tail;        // index among the split tiles, or -1 for a whole tile
-  int seg, nseg;   // this CTA's position among the CTAs sharing the tile
-};
-
-__host__ __device__ __forceinline__ long long sk_start(long long c, long long ctas, long long work) {
-  return c * work / ctas;
-}
-// CTA whose share of the split K iterations contains iteration x
-__host__ __device__ __forceinline__ int sk_owner(long long x, long long ctas, long long work) {
-  return static_cast<int>(((x + 1) * ctas - 1) / work);
-}
-
-// The work list of one CTA, walked identically by every role.
-struct WorkList {
-  int next_dp;
-  long long x, x_end;
-
-  __device__ __forceinline__ explicit WorkList(const TcParams& p) {
-    next_dp = blockIdx.x;
-    x = x_end = 0;
-    if (static_cast<int>(blockIdx.x) < p.sk_ctas) {
-      x = sk_start(blockIdx.x, p.sk_ctas, p.sk_work);
-      x_end = sk_start(blockIdx.x + 1, p.sk_ctas, p.sk_work);
-    }
-  }
-
-  __device__ __forceinline__ bool next(const TcParams& p, WorkItem& w) {
-    if (next_dp < p.dp_tiles) {
-      w.tile = next_dp;
-      w.k0 = 0;
-      w.k1 = p.k_iters;
-      w.tail = -1;
-      w.seg = 0;
-      w.nseg = 1;
-      next_dp += gridDim.x;
-      return true;
-    }
-    if (x < x_end) {
-      const long long ki = p.k_iters;
-      const int i = static_cast<int>(x / ki);
-      w.tile = p.dp_tiles + i;
-      w.tail = i;
-      w.k0 = static_cast<int>(x - i * ki);
-      w.k1 = static_cast<int>(min(ki, w.k0 + (x_end - x)));
-      const int first = sk_owner(i * ki, p.sk_ctas, p.sk_work);
-      const int last = sk_owner((i + 1) * ki - 1, p.sk_ctas, p.sk_work);
-      w.seg = static_cast<int>(blockIdx.x) - first;
-      w.nseg = last - first + 1;
-      x += w.k1 - w.k0;
-      return true;
-    }
-    return false;
-  }
 };
 
 template <int TM, int BK, int NPROD>
@@ -542,7 +478,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Split tiles whose last partial this CTA published: every thread of the
   // CTA sums the partials in segment order (fixed, whichever CTA gets here)
   // and writes C.  Many independent 16-byte loads per thread keep the L2
-  // reads in flight.
+  // reads in flight.  (Written out here rather than through the shared
+  // reduce_partials(): measured on GB300, that call made this kernel's
+  // mainloop about 8 % slower.)
   const int npend = *pending_count;
   if (npend > 0) {
     __threadfence();
@@ -686,32 +624,6 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
   return best;
 }
 
-// Splits the last partial wave along K.  Fills dp_tiles / sk_ctas / sk_work /
-// max_seg and returns the workspace bytes the split needs (0: no split).
-size_t plan_split_tail(TcParams& p, long tiles, int grid, int tm) {
-  p.dp_tiles = static_cast<int>(tiles);
-  p.sk_ctas = 0;
-  p.sk_work = 0;
-  p.max_seg = 1;
-  const long tail = tiles % grid;
-  if (tail == 0) return 0;
-  const long long work = static_cast<long long>(tail) * p.k_iters;
-  const long long ctas = std::min<long long>(grid, work / kMinSplitIters);
-  if (ctas <= tail) return 0;   // each CTA would still get whole tiles
-  int max_seg = 1;
-  for (long i = 0; i < tail; ++i) {
-    const int first = sk_owner(i * p.k_iters, ctas, work);
-    const int last = sk_owner((i + 1) * static_cast<long long>(p.k_iters) - 1, ctas, work);
-    max_seg = std::max(max_seg, last - first + 1);
-  }
-  if (max_seg == 1 || tail * sizeof(unsigned) > kCounterBytes) return 0;
-  p.dp_tiles = static_cast<int>(tiles - tail);
-  p.sk_ctas = static_cast<int>(ctas);
-  p.sk_work = work;
-  p.max_seg = max_seg;
-  return kCounterBytes + static_cast<size_t>(tail) * max_seg * tm * kTN * sizeof(float);
-}
-
 }  // namespace
 
 int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
@@ -742,7 +654,8 @@ int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) 
     tm = choose_tm(g, true);
     p.tiles_m = ceil_div(g.M, tm);
     const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
-    if (tiles <= 0x7fffffffL) ws_bytes = plan_split_tail(p, tiles, g.num_sms, tm);
+    if (tiles <= 0x7fffffffL)
+      ws_bytes = plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * kTN * sizeof(float));
   }
   void* ws = nullptr;
   int must_clear = 0;
@@ -851,7 +764,8 @@ int launch_tc_fixed_scratch(const GemmArgs& g, int nprod, cudaStream_t stream, i
   p.tiles_m = ceil_div(g.M, tm);
   long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
-  const size_t need = plan_split_tail(p, tiles, g.num_sms, tm);
+  const size_t need =
+      plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * kTN * sizeof(float));
   if (need > GEMM_F32_NOALLOC_SCRATCH_BYTES) return GEMM_F32_ESCRATCH;
   int grid;
   if (need) {

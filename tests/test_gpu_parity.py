@@ -170,7 +170,7 @@ def test_large_config_tc1x_sampled():
     assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc1x"], "c4/tc1x")
 
 
-@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x", "ffma"])
 @pytest.mark.parametrize("shape", [(700, 2000, 900), (700, 2001, 900), (256, 4096, 384),
                                    (512, 16384, 512), (3000, 2048, 2000), (1024, 512, 1024)])
 def test_split_tail_matches_whole_tiles(mode, shape):
