@@ -9,7 +9,7 @@ streams.
     C = g.matmul(A, B)                     # A, B: contiguous fp32 CUDA tensors
     g.gemm_f32(A, B, C, M, N, K, stream)   # the C-ABI call, same arguments
 """
-from ._binding import (FLAG_FORCE_STAGED, FLAG_TILE64, FLAG_TILE128, FLAG_TILE256,  # noqa: F401
+from ._binding import (FLAG_CTA_PAIR, FLAG_FORCE_STAGED, FLAG_SINGLE_CTA, FLAG_TILE64, FLAG_TILE128, FLAG_TILE256,  # noqa: F401
                        FLAG_NO_SPLIT_K, FLAG_ONE_TILE_PER_CTA, FLAG_TEST_DROP_COPY, GEMM_F32_EDEVICE, GEMM_F32_EINVAL,
                        GEMM_F32_ELAUNCH, GEMM_F32_ESCRATCH, GEMM_F32_ETIMEOUT, GEMM_F32_OK, LIB_PATH, MODE_FFMA,
                        MODE_TC1X, MODE_TC3X, MODES, GemmError, check, declared_symbols,

@@ -33,6 +33,8 @@ FLAG_TILE128 = 0x20
 FLAG_TILE256 = 0x40
 FLAG_ONE_TILE_PER_CTA = 0x100
 FLAG_NO_SPLIT_K = 0x200
+FLAG_CTA_PAIR = 0x400
+FLAG_SINGLE_CTA = 0x800
 FLAG_TEST_DROP_COPY = 0x1000
 
 _ERRORS = {

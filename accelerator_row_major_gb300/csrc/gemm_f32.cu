@@ -94,6 +94,7 @@ bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
 constexpr unsigned kKnownFlags = GEMM_F32_FLAG_FORCE_STAGED | GEMM_F32_FLAG_TILE64 |
                                  GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
                                  GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K |
+                                 GEMM_F32_FLAG_CTA_PAIR | GEMM_F32_FLAG_SINGLE_CTA |
                                  GEMM_F32_FLAG_TEST_DROP_COPY;
 
 }  // namespace
@@ -143,6 +144,7 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
   if (flags & ~kKnownFlags) return GEMM_F32_EINVAL;
   const unsigned bn_flags = flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256);
   if (bn_flags & (bn_flags - 1)) return GEMM_F32_EINVAL;  // at most one tile width
+  if ((flags & GEMM_F32_FLAG_CTA_PAIR) && (flags & GEMM_F32_FLAG_SINGLE_CTA)) return GEMM_F32_EINVAL;
   if (M == 0 || N == 0) return GEMM_F32_OK;
   const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
   const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * sizeof(float);

@@ -30,6 +30,11 @@ void* acquire_workspace(int device, cudaStream_t stream, size_t bytes, int* must
 // negative GEMM_F32_E* code.  *launches receives the kernels launched.
 int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 
+// Tensor-core path on CTA pairs (256 x 256 tiles, cta_group::2), and whether
+// a problem should take it (large M and N, or forced by flags).
+bool tc_pair_suits(const GemmArgs& g);
+int launch_tc_pair(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
+
 // Tensor-core path whose split-tail scratch comes from a fixed array inside
 // the library (no allocation).  Returns GEMM_F32_ESCRATCH if the product
 // would need more than GEMM_F32_NOALLOC_SCRATCH_BYTES.

@@ -627,6 +627,7 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
 }  // namespace
 
 int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+  if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
   *launches = 0;
   const int bk = nprod == 3 ? 16 : 32;
   TcParams p;

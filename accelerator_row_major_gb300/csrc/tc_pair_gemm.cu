@@ -1,0 +1,789 @@
+// Tensor-core FP32 GEMM on CTA pairs (tcgen05 cta_group::2) for sm_103a.
+//
+// Same product and the same 3xTF32 / 1xTF32 arithmetic as tc_gemm.cu
+// (C[i][j] = sum_k A[i][k] * B[k][j], row-major; "LeetGPU problem 2: matrix
+// multiplication", yekq.top, section "problem statement"), but each output
+// tile of 256 columns of C by 256 rows is computed by a cluster of two CTAs
+// on two SMs with one M = 256 MMA issued by the even CTA:
+//   - CTA r holds columns n0 + 128 r .. +127 of the tile: the transposed B
+//     tile's TF32 parts in its tensor memory (the MMA's A operand, 128
+//     lanes per CTA) and that half of the accumulator (128 lanes x 256
+//     columns = all 256 rows of C);
+//   - CTA r holds rows m0 + 128 r .. +127 of the A tile in shared memory
+//     (the MMA's B operand is split by rows across the pair, and the pair's
+//     tensor cores exchange the halves).
+// Against one CTA per 128 x 256 tile, every SM reads half as much of the A
+// tile from L2 and its shared memory serves half as many MMA operand bytes.
+//
+// Roles per CTA: warp 0 TMA producer (own halves); warp 1 TMEM allocation
+// (both CTAs, cta_group::2) and MMA issue (even CTA only); warps 2..3
+// forward finished stages to the even CTA; warps 4..7 epilogue (own
+// accumulator half); warps 8..15 transform (own halves).  The even CTA's MMA
+// waits for both CTAs' stages (one cluster-scope arrive per CTA and stage)
+// and for both epilogues to drain the accumulator; its commits arrive on
+// both CTAs' barriers (multicast).  Waits are bounded as in
+// tc_gemm.cu; the split tail of the last wave works per CTA half.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/gemm_f32.h"
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace gemm_f32_impl {
+using namespace gemm_f32_dev;
+
+namespace {
+
+constexpr int kHalf = 128;                   // rows of A / columns of C per CTA
+constexpr int kPairTile = 256;               // the pair's tile: 256 x 256
+constexpr int kWarps = 18;                   // 16 + two more forwarding warps
+constexpr int kThreads = kWarps * 32;
+constexpr int kForwarders = 4;               // warps 2, 3, 16, 17
+constexpr int kEpilogueWarp0 = 4;
+constexpr int kTransformWarp0 = 8;
+constexpr int kTransformWarps = 8;
+constexpr int kEpilogueWarps = 4;
+constexpr int kEpilogueBarrier = 1;
+constexpr int kSmemLimit = 232448;
+constexpr int kTmemCols = 512;
+constexpr int kRasterGroup = 8;
+constexpr int kMaxPending = 8;
+
+struct PairParams {
+  const float* A;
+  const float* B;
+  float* C;
+  int M, N, K;
+  int tiles_m, tiles_n, k_iters;     // tiles of 256 x 256
+  int dp_tiles, sk_ctas;             // split-tail plan over CTA pairs
+  long long sk_work;
+  int max_seg;
+  float* partials;                   // [tail][max_seg][2][256 m][128 n]
+  unsigned* counters;                // [tail][2]
+  int drop_first_copy;
+  unsigned* err;
+};
+
+template <int BK, int NPROD>
+struct PairCfg {
+  static constexpr int A_BYTES = kHalf * BK * 4;
+  static constexpr int A_LO_BYTES = NPROD == 3 ? A_BYTES : 0;
+  static constexpr int B_RAW_BYTES = BK * kHalf * 4;
+  static constexpr int STAGE_BYTES = A_BYTES + A_LO_BYTES + B_RAW_BYTES;
+  static constexpr int ACC_COLS = kPairTile;                       // one accumulator
+  static constexpr int BT_COLS = BK * (NPROD == 3 ? 2 : 1);
+  static constexpr int FIT_SMEM = (kSmemLimit - 2048) / STAGE_BYTES;
+  static constexpr int FIT_TMEM = (kTmemCols - ACC_COLS) / BT_COLS;
+  static constexpr int S0 = FIT_SMEM < FIT_TMEM ? FIT_SMEM : FIT_TMEM;
+  static constexpr int STAGES = S0 < 8 ? S0 : 8;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 1024;
+  static constexpr uint32_t A_SWZ_MASK = BK == 32 ? 7u : 3u;
+  static constexpr uint32_t A_LAYOUT = BK == 32 ? 2u : 4u;
+  static constexpr uint32_t A_SBO = BK == 32 ? 1024u : 512u;
+  static_assert(STAGES >= 2, "at least two stages");
+  static_assert(A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "1024-byte aligned atoms");
+  static_assert(ACC_COLS + STAGES * BT_COLS <= kTmemCols, "TMEM budget");
+};
+
+// ---------------------------------------------------------------- pair primitives
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// Every thread of both CTAs.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+// Non-blocking test: the waits below spin on it, since a blocking try_wait
+// on a barrier that another SM arrives on was measured to wake late.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// Bounded wait on a barrier that threads of the other CTA arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* err,
+                                                  unsigned site) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+      if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitBudgetNs) {
+      record_error(err, site);
+      return false;
+    }
+  }
+}
+
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// D (both CTAs' TMEM) (+)= A (both CTAs' TMEM lanes) * B (rows split across
+// both CTAs' shared memory).  Issued by the even CTA.
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::tf32 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The barrier at `bar` in both CTAs receives one arrive once the MMAs this
+// thread issued before have completed.
+__device__ __forceinline__ void mma_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
+      "[%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(0x3))
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t swizzle(uint32_t o, uint32_t mask) {
+  return o ^ (((o >> 7) & mask) << 4);
+}
+
+template <int NPROD>
+__device__ __forceinline__ void split_operand(uint32_t x, uint32_t& hi, uint32_t& lo) {
+  if (NPROD == 3) {
+    hi = x;
+    lo = tf32_lo_of_truncated(x);
+  } else {
+    hi = tf32_round_bits(x);
+    lo = 0u;
+  }
+}
+
+template <int NC>
+__device__ __forceinline__ void tmem_store_cols(uint32_t taddr, const uint32_t (&v)[NC]);
+template <>
+__device__ __forceinline__ void tmem_store_cols<8>(uint32_t taddr, const uint32_t (&v)[8]) {
+  tmem_st_8cols(taddr, v);
+}
+template <>
+__device__ __forceinline__ void tmem_store_cols<16>(uint32_t taddr, const uint32_t (&v)[16]) {
+  tmem_st_16cols(taddr, v);
+}
+
+__device__ __forceinline__ void epilogue_sync() {
+  asm volatile("bar.sync %0, %1;" ::"r"(kEpilogueBarrier), "r"(kEpilogueWarps * 32) : "memory");
+}
+
+__device__ __forceinline__ bool epilogue_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(kEpilogueBarrier), "r"(kEpilogueWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+// The work list of a CTA pair: as WorkList, with the pair as the unit.
+struct PairWorkList {
+  int unit, units, next_dp;
+  long long x, x_end;
+
+  __device__ __forceinline__ explicit PairWorkList(const PairParams& p) {
+    unit = static_cast<int>(blockIdx.x >> 1);
+    units = static_cast<int>(gridDim.x >> 1);
+    next_dp = unit;
+    x = x_end = 0;
+    if (unit < p.sk_ctas) {
+      x = sk_start(unit, p.sk_ctas, p.sk_work);
+      x_end = sk_start(unit + 1, p.sk_ctas, p.sk_work);
+    }
+  }
+
+  __device__ __forceinline__ bool next(const PairParams& p, WorkItem& w) {
+    if (next_dp < p.dp_tiles) {
+      w.tile = next_dp;
+      w.k0 = 0;
+      w.k1 = p.k_iters;
+      w.tail = -1;
+      w.seg = 0;
+      w.nseg = 1;
+      next_dp += units;
+      return true;
+    }
+    if (x < x_end) {
+      const long long ki = p.k_iters;
+      const int i = static_cast<int>(x / ki);
+      w.tile = p.dp_tiles + i;
+      w.tail = i;
+      w.k0 = static_cast<int>(x - i * ki);
+      w.k1 = static_cast<int>(min(ki, w.k0 + (x_end - x)));
+      const int first = sk_owner(i * ki, p.sk_ctas, p.sk_work);
+      const int last = sk_owner((i + 1) * ki - 1, p.sk_ctas, p.sk_work);
+      w.seg = unit - first;
+      w.nseg = last - first + 1;
+      x += w.k1 - w.k0;
+      return true;
+    }
+    return false;
+  }
+};
+
+template <int BK, int NPROD, bool TMA>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const PairParams p) {
+  using Cfg = PairCfg<BK, NPROD>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_dyn[];
+  const uint32_t dyn0 = smem_addr(smem_dyn);
+  const uint32_t base = (dyn0 + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_dyn + (base - dyn0);
+  const uint32_t bars = base + S * Cfg::STAGE_BYTES;
+  auto full_bar = [&](int s) { return bars + 8u * s; };              // own TMA landed
+  auto ready_bar = [&](int s) { return bars + 8u * (S + s); };       // both CTAs split (even CTA's)
+  auto empty_bar = [&](int s) { return bars + 8u * (2 * S + s); };   // pair MMAs done with stage
+  auto done_bar = [&](int s) { return bars + 8u * (3 * S + s); };    // own transform finished stage
+  const uint32_t accf_bar = bars + 8u * (4 * S);                     // accumulator complete
+  const uint32_t acce_bar = bars + 8u * (4 * S + 1);                 // both halves drained (even CTA's)
+  const uint32_t drain_bar = bars + 8u * (4 * S + 2);
+  const uint32_t tmem_slot = bars + 8u * (4 * S + 3);
+  volatile int* const pending_count =
+      reinterpret_cast<volatile int*>(base_ptr + (tmem_slot + 8u - base));
+  WorkItem* const pending = reinterpret_cast<WorkItem*>(base_ptr + (tmem_slot + 16u - base));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+
+  if (threadIdx.x == 0) {
+    *pending_count = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(ready_bar(s), 2);   // one arrive per CTA (from its forwarding warp)
+      mbar_init(empty_bar(s), 1);
+      mbar_init(done_bar(s), kTransformWarps * 32);
+    }
+    mbar_init(accf_bar, 1);
+    mbar_init(acce_bar, 2 * kEpilogueWarps);
+    mbar_init(drain_bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  if (TMA && warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();      // barriers of both CTAs exist before any remote arrive
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+
+  WorkItem w;
+  if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer (own halves)
+    if (TMA && lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t armed = 0, last_ph = 0;
+      bool ok = true, first = true;
+      PairWorkList list(p);
+      while (ok && list.next(p, w)) {
+        const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+        for (int kt = w.k0; kt < w.k1; ++kt) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t st = base + s * Cfg::STAGE_BYTES;
+          if (p.drop_first_copy && blockIdx.x == 0 && first) {
+            first = false;   // test hook: this stage is never filled
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
+            continue;
+          }
+          first = false;
+          mbar_arrive_expect_tx(full_bar(s), Cfg::A_BYTES + Cfg::B_RAW_BYTES);
+          armed |= 1u << s;
+          last_ph = (last_ph & ~(1u << s)) | (ph << s);
+          tma_load_2d(st, &tmA, full_bar(s), kt * BK, c.tm * kPairTile + static_cast<int>(rank) * kHalf);
+          tma_load_2d(st + Cfg::A_BYTES + Cfg::A_LO_BYTES, &tmB, full_bar(s),
+                      c.tn * kPairTile + static_cast<int>(rank) * kHalf, kt * BK);
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      for (int q = 0; q < S; ++q)
+        if (armed & (1u << q)) mbar_wait(full_bar(q), (last_ph >> q) & 1u, p.err, kSiteDrainTma);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    if (rank == 0 && lane == 0) {
+      constexpr uint32_t idesc = idesc_tf32(2 * kHalf, kPairTile, false, false);
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t acc_ph = 0;
+      bool ok = true;
+      PairWorkList list(p);
+      while (ok && list.next(p, w)) {
+        if (!mbar_wait_cluster(acce_bar, acc_ph ^ 1u, p.err, kSiteMmaAccEmpty)) break;
+        tc_fence_after_sync();
+        for (int kt = w.k0; kt < w.k1; ++kt) {
+          if (!mbar_wait_cluster(ready_bar(s), ph, p.err, kSiteMmaReady)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t st = base + s * Cfg::STAGE_BYTES;
+          const uint32_t bt = tmem_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS);
+#pragma unroll
+          for (int kk = 0; kk < BK / 8; ++kk) {
+            const uint64_t a_hi = smem_desc(st + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
+            mma_pair(tmem_base, bt + kk * 8, a_hi, idesc, (kt > w.k0 || kk > 0) ? 1u : 0u);
+            if (NPROD == 3) {
+              const uint64_t a_lo =
+                  smem_desc(st + Cfg::A_BYTES + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
+              mma_pair(tmem_base, bt + kk * 8, a_lo, idesc, 1u);
+              mma_pair(tmem_base, bt + BK + kk * 8, a_hi, idesc, 1u);
+            }
+          }
+          mma_commit_both(empty_bar(s));
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit_both(accf_bar);
+        acc_ph ^= 1u;
+      }
+      mma_commit_local(drain_bar);
+      mbar_wait(drain_bar, 0, p.err, kSiteDrainMma);
+    }
+    __syncwarp();
+  } else if (warp == 2 || warp == 3 || warp >= 16) {
+    // ------------------------------------------------------------ forwarders
+    // A cluster-scope release arrive takes about as long as a stage of MMAs
+    // when the arriving thread has just written the stage; these warps, with
+    // nothing of their own to publish, pass each stage's completion on to the
+    // even CTA (stage i by forwarder i mod 4) off the transform path.
+    if (lane == 0) {
+      const uint32_t leader_ready0 = map_rank(ready_bar(0), 0);
+      const uint32_t mine = static_cast<uint32_t>(warp < 16 ? warp - 2 : warp - 14);
+      int s = 0;
+      uint32_t ph = 0, count = 0;
+      bool ok = true;
+      PairWorkList list(p);
+      while (ok && list.next(p, w)) {
+        for (int kt = w.k0; kt < w.k1; ++kt, ++count) {
+          if (count % kForwarders == mine) {
+            if (!mbar_wait(done_bar(s), ph, p.err, kSiteTransformFull)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_cluster(leader_ready0 + 8u * s);
+          }
+          if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + kEpilogueWarps) {
+    // ------------------------------------------------------------ epilogue (own half)
+    const int q = warp & 3;
+    const int nl = q * 32 + lane;
+    const uint32_t leader_acce = map_rank(acce_bar, 0);
+    uint32_t acc_ph = 0;
+    PairWorkList list(p);
+    while (list.next(p, w)) {
+      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      if (!epilogue_all(mbar_wait(accf_bar, acc_ph, p.err, kSiteEpilogueFull))) break;
+      tc_fence_after_sync();
+      const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+      const int n = c.tn * kPairTile + static_cast<int>(rank) * kHalf + nl;
+      const bool n_ok = n < p.N;
+      if (w.nseg > 1) {
+        float* const mine =
+            p.partials +
+            ((static_cast<size_t>(w.tail) * p.max_seg + w.seg) * 2 + rank) * (kPairTile * kHalf) + nl;
+#pragma unroll 1
+        for (int chunk = 0; chunk < kPairTile / 32; ++chunk) {
+          uint32_t v[32];
+          tmem_ld_32cols(t_acc + chunk * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * kHalf] = __uint_as_float(v[j]);
+        }
+        __threadfence();
+        epilogue_sync();
+        if (nl == 0 &&
+            atomicAdd(p.counters + 2 * w.tail + rank, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+          if (*pending_count < kMaxPending)
+            pending[(*pending_count)++] = w;
+          else
+            record_error(p.err, kSitePendingOverflow);
+        }
+      } else {
+#pragma unroll 1
+        for (int chunk = 0; chunk < kPairTile / 32; ++chunk) {
+          uint32_t v[32];
+          tmem_ld_32cols(t_acc + chunk * 32, v);
+          tmem_wait_ld();
+          const int m0 = c.tm * kPairTile + chunk * 32;
+          if (n_ok) {
+            float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(p.N) + n;
+            const int rows = min(32, p.M - m0);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < rows) dst[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+          }
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_acce);
+      acc_ph ^= 1u;
+    }
+  } else if (warp >= kTransformWarp0 && warp < kTransformWarp0 + kTransformWarps) {
+    // ------------------------------------------------------------ transform (own halves)
+    constexpr int KH = BK / 2;
+    const int tt = threadIdx.x - kTransformWarp0 * 32;
+    const int col = tt & 127;
+    const int kh0 = (tt >> 7) * KH;
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(col & ~31) << 16);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    PairWorkList list(p);
+    while (ok && list.next(p, w)) {
+      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      for (int kt = w.k0; kt < w.k1; ++kt) {
+        uint8_t* const st = base_ptr + s * Cfg::STAGE_BYTES;
+        if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteTransformEmpty)) {
+          ok = false;
+          break;
+        }
+        if (TMA && !mbar_wait(full_bar(s), ph, p.err, kSiteTransformFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t bh[KH], bl[KH];
+        if (TMA) {
+          uint4* const hi = reinterpret_cast<uint4*>(st);
+          uint4* const lo = reinterpret_cast<uint4*>(st + Cfg::A_BYTES);
+#pragma unroll 4
+          for (int i = tt; i < Cfg::A_BYTES / 16; i += kTransformWarps * 32) {
+            const uint4 x = hi[i];
+            if (NPROD == 3) {
+              lo[i] = make_uint4(tf32_lo_of_truncated(x.x), tf32_lo_of_truncated(x.y),
+                                 tf32_lo_of_truncated(x.z), tf32_lo_of_truncated(x.w));
+            } else {
+              hi[i] = make_uint4(tf32_round_bits(x.x), tf32_round_bits(x.y), tf32_round_bits(x.z),
+                                 tf32_round_bits(x.w));
+            }
+          }
+          const uint32_t* braw =
+              reinterpret_cast<const uint32_t*>(st + Cfg::A_BYTES + Cfg::A_LO_BYTES);
+#pragma unroll
+          for (int k = 0; k < KH; ++k) split_operand<NPROD>(braw[(kh0 + k) * kHalf + col], bh[k], bl[k]);
+        } else {
+          const int m0 = c.tm * kPairTile + static_cast<int>(rank) * kHalf;
+          const int n0 = c.tn * kPairTile + static_cast<int>(rank) * kHalf;
+          const int k0 = kt * BK;
+#pragma unroll 2
+          for (int e = tt; e < kHalf * BK; e += kTransformWarps * 32) {
+            const int r = e / BK, k = e % BK;
+            const int gm = m0 + r, gk = k0 + k;
+            const uint32_t x = (gm < p.M && gk < p.K)
+                                   ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
+                                   : 0u;
+            uint32_t h, l;
+            split_operand<NPROD>(x, h, l);
+            const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
+            *reinterpret_cast<uint32_t*>(st + o) = h;
+            if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+          }
+          const int gn = n0 + col;
+#pragma unroll
+          for (int k = 0; k < KH; ++k) {
+            const int gk = k0 + kh0 + k;
+            const uint32_t x = (gn < p.N && gk < p.K)
+                                   ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
+                                   : 0u;
+            split_operand<NPROD>(x, bh[k], bl[k]);
+          }
+        }
+        const uint32_t bt =
+            lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS + kh0);
+        tmem_store_cols<KH>(bt, bh);
+        if (NPROD == 3) tmem_store_cols<KH>(bt + BK, bl);
+        tmem_wait_st();
+        fence_proxy_async_smem();   // A hi/lo: generic-proxy writes -> tensor-core reads
+        tc_fence_before_sync();
+        mbar_arrive(done_bar(s));   // local; a forwarding warp tells the even CTA
+        if (++s == S) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync();   // the even CTA's MMAs have finished with this CTA's memory
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  // Split tiles whose last partial (of this CTA's half) this CTA published:
+  // every thread sums the partials in segment order and writes C.
+  const int npend = *pending_count;
+  if (npend > 0) {
+    __threadfence();
+    for (int e = 0; e < npend; ++e) {
+      const WorkItem pw = pending[e];
+      const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      const float4* const parts = reinterpret_cast<const float4*>(p.partials) +
+                                  static_cast<size_t>(pw.tail) * p.max_seg * 2 * (kPairTile * kHalf / 4);
+      constexpr int kVec = kPairTile * kHalf / 4;   // float4s of one half partial
+      constexpr int kBatch = 8;                     // float4s per thread in flight
+#pragma unroll 1
+      for (int base = 0; base < kVec; base += kBatch * kThreads) {
+        float4 sum[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int sg = 0; sg < pw.nseg; ++sg) {
+          const float4* src = parts + (static_cast<size_t>(sg) * 2 + rank) * kVec;
+          float4 x[kBatch];
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            const int f = base + threadIdx.x + i * kThreads;
+            x[i] = f < kVec ? __ldcg(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < kBatch; ++i) {
+            sum[i].x += x[i].x;
+            sum[i].y += x[i].y;
+            sum[i].z += x[i].z;
+            sum[i].w += x[i].w;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int f = base + threadIdx.x + i * kThreads;   // float4 index in the half tile
+          if (f >= kVec) continue;
+          const int m = c.tm * kPairTile + f / (kHalf / 4);
+          const int n = c.tn * kPairTile + static_cast<int>(rank) * kHalf + (f % (kHalf / 4)) * 4;
+          if (m < p.M) {
+            float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n;
+            const float vals[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq)
+              if (n + qq < p.N) dst[qq] = vals[qq];
+          }
+        }
+      }
+      if (threadIdx.x == 0) p.counters[2 * pw.tail + rank] = 0;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_cols, int box_rows,
+               CUtensorMapSwizzle swz) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      (void)cudaGetLastError();
+  });
+  if (!g_encode) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4u};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+
+template <int BK, int NPROD, bool TMA>
+int launch_pair_one(const GemmArgs& g, const PairParams& p, const CUtensorMap& ma,
+                    const CUtensorMap& mb, int grid, cudaStream_t stream) {
+  using Cfg = PairCfg<BK, NPROD>;
+  static std::atomic<unsigned long long> configured{0};
+  auto kern = tc_pair_kernel<BK, NPROD, TMA>;
+  const unsigned long long bit = 1ull << (g.device % kMaxDevices);
+  if (!(configured.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
+        cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
+    configured.fetch_or(bit);
+  }
+  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  return GEMM_F32_OK;
+}
+
+}  // namespace
+
+bool tc_pair_suits(const GemmArgs& g) {
+  if (g.flags & GEMM_F32_FLAG_SINGLE_CTA) return false;
+  if (g.flags & GEMM_F32_FLAG_CTA_PAIR) return true;
+  if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
+                 GEMM_F32_FLAG_ONE_TILE_PER_CTA))
+    return false;
+  const long tiles = static_cast<long>((g.M + kPairTile - 1) / kPairTile) *
+                     ((g.N + kPairTile - 1) / kPairTile);
+  return g.M >= kPairTile && g.N >= kPairTile && tiles >= g.num_sms / 2;
+}
+
+int launch_tc_pair(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+  *launches = 0;
+  const int bk = nprod == 3 ? 16 : 32;
+  const int pairs = g.num_sms / 2;
+  if (pairs < 1) return GEMM_F32_EDEVICE;
+  PairParams p;
+  p.A = g.A;
+  p.B = g.B;
+  p.C = g.C;
+  p.M = g.M;
+  p.N = g.N;
+  p.K = g.K;
+  p.tiles_m = (g.M + kPairTile - 1) / kPairTile;
+  p.tiles_n = (g.N + kPairTile - 1) / kPairTile;
+  p.k_iters = (g.K + bk - 1) / bk;
+  p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
+  p.err = g.err;
+  p.partials = nullptr;
+  p.counters = nullptr;
+  const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
+  if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
+  p.dp_tiles = static_cast<int>(tiles);
+  p.sk_ctas = 0;
+  p.sk_work = 0;
+  p.max_seg = 1;
+  int units = static_cast<int>(std::min<long>(tiles, pairs));
+  if (!(g.flags & GEMM_F32_FLAG_NO_SPLIT_K)) {
+    PairParams q = p;
+    const size_t ws_bytes =
+        plan_split_tail(q, tiles, pairs, sizeof(float) * 2 * kPairTile * kHalf);
+    int must_clear = 0;
+    void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes, &must_clear) : nullptr;
+    if (ws) {
+      p = q;
+      units = pairs;
+      p.counters = static_cast<unsigned*>(ws);
+      p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
+      if (must_clear) {
+        if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
+          (void)cudaGetLastError();
+          return GEMM_F32_ELAUNCH;
+        }
+        *launches += 1;
+      }
+    }
+  }
+  const int grid = 2 * units;
+
+  bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && g.K % 4 == 0 && g.N % 4 == 0 &&
+             reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
+             reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+  alignas(64) CUtensorMap ma, mb;
+  if (tma) {
+    tma = encode_2d(&ma, g.A, g.M, g.K, bk, kHalf,
+                    bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
+          encode_2d(&mb, g.B, g.K, g.N, kHalf, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!tma) {
+    memset(&ma, 0, sizeof(ma));
+    memset(&mb, 0, sizeof(mb));
+  }
+  int rc;
+  if (nprod == 3)
+    rc = tma ? launch_pair_one<16, 3, true>(g, p, ma, mb, grid, stream)
+             : launch_pair_one<16, 3, false>(g, p, ma, mb, grid, stream);
+  else
+    rc = tma ? launch_pair_one<32, 1, true>(g, p, ma, mb, grid, stream)
+             : launch_pair_one<32, 1, false>(g, p, ma, mb, grid, stream);
+  if (rc == GEMM_F32_OK) *launches += 1;
+  return rc;
+}
+
+}  // namespace gemm_f32_impl

@@ -85,8 +85,13 @@ enum gemm_f32_mode {
 #define GEMM_F32_FLAG_TILE256 0x40u      /*   columns); default: chosen by size */
 #define GEMM_F32_FLAG_ONE_TILE_PER_CTA 0x100u /* launch one CTA per output
                                             tile instead of the persistent grid */
-#define GEMM_F32_FLAG_NO_SPLIT_K 0x200u  /* tensor modes: never split the last
-                                            wave along K (no workspace)      */
+#define GEMM_F32_FLAG_NO_SPLIT_K 0x200u  /* never split the last wave along K
+                                            (no workspace)                    */
+#define GEMM_F32_FLAG_CTA_PAIR 0x400u    /* tensor modes: compute 256 x 256
+                                            tiles on pairs of SMs (cluster of
+                                            two CTAs, one M = 256 MMA); the
+                                            default for large M and N         */
+#define GEMM_F32_FLAG_SINGLE_CTA 0x800u  /* tensor modes: one CTA per tile    */
 #define GEMM_F32_FLAG_TEST_DROP_COPY 0x1000u /* testing only, tensor modes on
                                             the TMA path: CTA 0 never issues
                                             its first operand copy, so its

@@ -16,8 +16,8 @@ from tests._gpu import TOL, assert_close, lib, oracle_full, run_abi
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
-def test_lost_copy_reports_timeout_and_context_survives(mode):
+@pytest.mark.parametrize("mode,extra", [("tc3x", 0), ("tc1x", 0), ("tc3x", 0x400)])
+def test_lost_copy_reports_timeout_and_context_survives(mode, extra):
     import torch
 
     g = lib()
@@ -28,7 +28,7 @@ def test_lost_copy_reports_timeout_and_context_survives(mode):
     C = torch.empty((256, 256), dtype=torch.float32, device=dev)
     s = torch.cuda.current_stream(dev)
     t0 = time.time()
-    rc = g.gemm_f32_ex(At, Bt, C, 256, 256, 64, mode, g.FLAG_TEST_DROP_COPY, s)
+    rc = g.gemm_f32_ex(At, Bt, C, 256, 256, 64, mode, g.FLAG_TEST_DROP_COPY | extra, s)
     assert rc == g.GEMM_F32_OK
     st, site = g.gemm_f32_status(s)
     elapsed = time.time() - t0

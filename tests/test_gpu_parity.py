@@ -19,6 +19,8 @@ FLAG_STAGED = 0x1
 FLAG_TILE = {64: 0x10, 128: 0x20, 256: 0x40}
 FLAG_ONE_TILE = 0x100
 FLAG_NO_SPLIT = 0x200
+FLAG_PAIR = 0x400
+FLAG_SINGLE = 0x800
 
 
 @pytest.fixture(scope="module")
@@ -197,3 +199,38 @@ def test_split_tail_on_two_streams_and_after_release():
     assert g.gemm_f32_release() == g.GEMM_F32_OK
     C, _ = run_abi(A, B, "tc3x")
     assert_close(C, Co, absAB, TOL["tc3x"], "after release")
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("staged", [False, True])
+@pytest.mark.parametrize("shape", [(1024, 512, 1024), (1001, 513, 777), (300, 264, 200),
+                                   (700, 2000, 900), (3000, 2048, 2000), (129, 33, 257)])
+def test_cta_pair_path(mode, staged, shape):
+    """256 x 256 tiles on CTA pairs (cta_group::2), forced on any shape."""
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "uniform", 3 * M + K)
+    Co, absAB = oracle_full(A, B)
+    flags = FLAG_PAIR | (FLAG_STAGED if staged else 0)
+    C, outs = run_abi(A, B, mode, flags, repeats=2)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert_close(C, Co, absAB, TOL[mode], "pair %s/%s/staged%d" % (shape, mode, staged))
+    C, _ = run_abi(A, B, mode, flags | FLAG_NO_SPLIT)
+    assert_close(C, Co, absAB, TOL[mode], "pair whole tiles %s/%s/staged%d" % (shape, mode, staged))
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+def test_cta_pair_integer_bit_exact(mode):
+    A, B = workloads.make_inputs(1024, 512, 1024, "int8", 12)
+    Co, _ = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode, FLAG_PAIR)
+    assert_bit_exact(C, Co, "pair int/%s" % mode)
+
+
+def test_single_and_pair_agree_on_a_large_problem():
+    A, B = workloads.make_inputs(2048, 1024, 2048, "normal", 21)
+    C_pair, _ = run_abi(A, B, "tc3x", FLAG_PAIR)
+    C_single, _ = run_abi(A, B, "tc3x", FLAG_SINGLE)
+    rows, cols = sample_indices(2048, 2048, 3000, 5)
+    vals, absv = oracle.gemm_entries(A, B, rows, cols)
+    for C in (C_pair, C_single):
+        assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc3x"], "pair/single")
