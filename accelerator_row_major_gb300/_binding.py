@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_last_launches.restype = ci
     lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
     lib.gemm_f32_noalloc.restype = ci
+    lib.gemm_f32_last_kernel.argtypes = []
+    lib.gemm_f32_last_kernel.restype = ctypes.c_char_p
     lib.gemm_f32_release.argtypes = []
     lib.gemm_f32_release.restype = ci
     lib.gemm_f32_version.argtypes = []
@@ -138,6 +140,11 @@ def gemm_f32_status(stream=None):
 
 def gemm_f32_last_launches() -> int:
     return lib().gemm_f32_last_launches()
+
+
+def gemm_f32_last_kernel() -> str:
+    """Kernel the last successful call on this thread launched."""
+    return lib().gemm_f32_last_kernel().decode()
 
 
 def gemm_f32_release() -> int:

@@ -313,7 +313,7 @@ int launch_vec(const GemmArgs& g, const FfmaParams& p, int grid, cudaStream_t st
 
 }  // namespace
 
-int launch_ffma(const GemmArgs& g, cudaStream_t stream, int* launches) {
+int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
   *launches = 0;
   FfmaParams p;
   p.A = g.A;
@@ -359,7 +359,10 @@ int launch_ffma(const GemmArgs& g, cudaStream_t stream, int* launches) {
   const bool vec = g.K % 4 == 0 && g.N % 4 == 0 && reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
   const int rc = vec ? launch_vec<true>(g, p, grid, stream) : launch_vec<false>(g, p, grid, stream);
-  if (rc == GEMM_F32_OK) *launches += 1;
+  if (rc == GEMM_F32_OK) {
+    *launches += 1;
+    g.kernel = "ffma_gemm_kernel";
+  }
   return rc;
 }
 

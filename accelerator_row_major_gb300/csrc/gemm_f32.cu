@@ -38,6 +38,7 @@ struct DeviceState {
 
 DeviceState g_devices[kMaxDevices];
 thread_local int t_last_launches = 0;
+thread_local const char* t_last_kernel = "none";
 
 // Set-up runs once per device, with that device current: checks it is an
 // sm_103 part, reads the SM count, takes the address of the error word and
@@ -137,6 +138,7 @@ void* gemm_f32_impl::acquire_workspace(int device, cudaStream_t stream, size_t b
 extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
                            unsigned flags, gemm_f32_stream_t stream_handle) {
   t_last_launches = 0;
+  t_last_kernel = "none";
   // ---- host-only checks first: no CUDA call for a malformed request
   if (M < 0 || N < 0 || K < 0) return GEMM_F32_EINVAL;
   if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_FFMA && mode != GEMM_F32_MODE_TC1X)
@@ -167,6 +169,7 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
       return GEMM_F32_ELAUNCH;
     }
     t_last_launches = 1;
+    t_last_kernel = "memset";
     return GEMM_F32_OK;
   }
 
@@ -187,7 +190,10 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
     rc = gemm_f32_impl::launch_ffma(g, stream, &launches);
   else
     rc = gemm_f32_impl::launch_tc(g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream, &launches);
-  if (rc == GEMM_F32_OK) t_last_launches = launches;
+  if (rc == GEMM_F32_OK) {
+    t_last_launches = launches;
+    t_last_kernel = g.kernel;
+  }
   return rc;
 }
 
@@ -199,6 +205,7 @@ extern "C" int gemm_f32(const float* A, const float* B, float* C, int M, int N, 
 extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                                 int mode, gemm_f32_stream_t stream_handle) {
   t_last_launches = 0;
+  t_last_kernel = "none";
   if (M < 0 || N < 0 || K < 0) return GEMM_F32_EINVAL;
   if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_TC1X) return GEMM_F32_EINVAL;
   if (M == 0 || N == 0) return GEMM_F32_OK;
@@ -222,6 +229,7 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
       return GEMM_F32_ELAUNCH;
     }
     t_last_launches = 1;
+    t_last_kernel = "memset";
     return GEMM_F32_OK;
   }
   gemm_f32_impl::GemmArgs g;
@@ -238,7 +246,10 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
   int launches = 0;
   const int rc = gemm_f32_impl::launch_tc_fixed_scratch(
       g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream, &launches);
-  if (rc == GEMM_F32_OK) t_last_launches = launches;
+  if (rc == GEMM_F32_OK) {
+    t_last_launches = launches;
+    t_last_kernel = g.kernel;
+  }
   return rc;
 }
 
@@ -283,5 +294,7 @@ extern "C" int gemm_f32_release(void) {
 }
 
 extern "C" int gemm_f32_last_launches(void) { return t_last_launches; }
+
+extern "C" const char* gemm_f32_last_kernel(void) { return t_last_kernel; }
 
 extern "C" const char* gemm_f32_version(void) { return "gemm_f32 1.0 sm_103a"; }

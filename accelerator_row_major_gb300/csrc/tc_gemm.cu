@@ -626,7 +626,7 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
 
 }  // namespace
 
-int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
   *launches = 0;
   const int bk = nprod == 3 ? 16 : 32;
@@ -711,7 +711,10 @@ int launch_tc(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) 
     rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
              : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
   }
-  if (rc == GEMM_F32_OK) *launches += 1;
+  if (rc == GEMM_F32_OK) {
+    *launches += 1;
+    g.kernel = "tc_gemm_kernel";
+  }
   return rc;
 }
 
@@ -732,7 +735,7 @@ FixedScratch g_fixed[kMaxDevices];
 
 }  // namespace
 
-int launch_tc_fixed_scratch(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   *launches = 0;
   if (g.device < 0 || g.device >= kMaxDevices) return GEMM_F32_EDEVICE;
   // In host code g_fixed_scratch only names the array; its device address is
@@ -812,7 +815,10 @@ int launch_tc_fixed_scratch(const GemmArgs& g, int nprod, cudaStream_t stream, i
     rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
              : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
   }
-  if (rc == GEMM_F32_OK) *launches += 1;
+  if (rc == GEMM_F32_OK) {
+    *launches += 1;
+    g.kernel = "tc_gemm_kernel";
+  }
   return rc;
 }
 

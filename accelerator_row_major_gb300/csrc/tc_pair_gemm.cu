@@ -714,7 +714,7 @@ bool tc_pair_suits(const GemmArgs& g) {
   return g.M >= kPairTile && g.N >= kPairTile && tiles >= g.num_sms / 2;
 }
 
-int launch_tc_pair(const GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   *launches = 0;
   const int bk = nprod == 3 ? 16 : 32;
   const int pairs = g.num_sms / 2;
@@ -782,7 +782,10 @@ int launch_tc_pair(const GemmArgs& g, int nprod, cudaStream_t stream, int* launc
   else
     rc = tma ? launch_pair_one<32, 1, true>(g, p, ma, mb, grid, stream)
              : launch_pair_one<32, 1, false>(g, p, ma, mb, grid, stream);
-  if (rc == GEMM_F32_OK) *launches += 1;
+  if (rc == GEMM_F32_OK) {
+    *launches += 1;
+    g.kernel = "tc_pair_kernel";
+  }
   return rc;
 }
 

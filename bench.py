@@ -280,6 +280,7 @@ def run_ours(args):
         for _ in range(max(3, args.warmup)):
             step()
     launches_per_step = g.gemm_f32_last_launches()
+    kernel = g.gemm_f32_last_kernel()
     rc, site = g.gemm_f32_status(stream)
     if rc != 0:
         raise SystemExit("device error word %d after warm-up" % site)
@@ -357,7 +358,6 @@ def run_ours(args):
 
     peaks, peak_src = measured_peaks()
     t_kernel = ms_per_step / 1e3  # one launch per step
-    kernel = "ffma_gemm_kernel" if args.mode == "ffma" else "tc_gemm_kernel"
     if args.mode == "ffma":
         peak = FFMA_FLOP_PER_SM_CLK * torch.cuda.get_device_properties(device).multi_processor_count \
             * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12

@@ -124,6 +124,12 @@ int gemm_f32_status(gemm_f32_stream_t stream, unsigned* site);
  * workspace had to be re-zeroed first). */
 int gemm_f32_last_launches(void);
 
+/* Name of the kernel the last successful call on this host thread launched:
+ * "tc_pair_kernel" (tensor cores, 256 x 256 tiles on SM pairs),
+ * "tc_gemm_kernel" (tensor cores, one SM per tile), "ffma_gemm_kernel",
+ * "memset" (K == 0) or "none" (nothing launched).  Static string. */
+const char* gemm_f32_last_kernel(void);
+
 /* Frees the current device's workspaces after synchronising the device.
  * Returns 0, or GEMM_F32_EDEVICE / GEMM_F32_ELAUNCH on a CUDA error. */
 int gemm_f32_release(void);

@@ -22,7 +22,8 @@ def g():
 def test_header_declares_the_entry_points(g):
     names = g.declared_symbols()
     assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status",
-                            "gemm_f32_last_launches", "gemm_f32_noalloc", "gemm_f32_release",
+                            "gemm_f32_last_kernel", "gemm_f32_last_launches", "gemm_f32_noalloc",
+                            "gemm_f32_release",
                             "gemm_f32_version"])
 
 
@@ -66,6 +67,7 @@ def test_malformed_requests_are_rejected_on_the_host(g, args, mode, flags):
 def test_empty_outputs_are_a_no_op(g):
     # M == 0 or N == 0: nothing to write, no CUDA call, success
     assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 0, 5, 5) == g.GEMM_F32_OK
+    assert g.gemm_f32_last_kernel() == "none"
     assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 5, 0, 5) == g.GEMM_F32_OK
     assert g.gemm_f32_ex(0, 0, 0, 0, 0, 0) == g.GEMM_F32_OK
     assert g.gemm_f32_last_launches() == 0

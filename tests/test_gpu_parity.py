@@ -234,3 +234,23 @@ def test_single_and_pair_agree_on_a_large_problem():
     vals, absv = oracle.gemm_entries(A, B, rows, cols)
     for C in (C_pair, C_single):
         assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc3x"], "pair/single")
+
+
+def test_last_kernel_names_the_path():
+    import torch
+    from tests._gpu import lib
+    g = lib()
+    dev = torch.device("cuda:0")
+    # 4096 x 4096 gives 256 tiles of 256 x 256: the pair path by default
+    A = torch.zeros((4096, 64), device=dev)
+    B = torch.zeros((64, 4096), device=dev)
+    C = torch.empty((4096, 4096), device=dev)
+    s = torch.cuda.current_stream(dev)
+    for mode, flags, want in (("tc3x", 0, "tc_pair_kernel"), ("tc3x", FLAG_SINGLE, "tc_gemm_kernel"),
+                              ("tc1x", 0, "tc_pair_kernel"), ("ffma", 0, "ffma_gemm_kernel")):
+        assert g.gemm_f32_ex(A, B, C, 4096, 4096, 64, mode, flags, s) == 0
+        assert g.gemm_f32_last_kernel() == want, (mode, flags)
+    assert g.gemm_f32_ex(A, B, C, 4096, 4096, 0, "tc3x", 0, s) == 0
+    assert g.gemm_f32_last_kernel() == "memset"
+    assert g.gemm_f32_status(s) == (0, 0)
+    assert not C.any()
