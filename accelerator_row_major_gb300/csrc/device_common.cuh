@@ -133,7 +133,8 @@ struct WorkList {
 // sk_work / max_seg (p.k_iters must be set) and returns the workspace bytes
 // the split needs, 0 when whole tiles are better (no split).
 template <class P>
-inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_bytes) {
+inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_bytes,
+                              int min_iters = kMinSplitIters) {
   p.dp_tiles = static_cast<int>(tiles);
   p.sk_ctas = 0;
   p.sk_work = 0;
@@ -141,7 +142,7 @@ inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_by
   const long tail = tiles % grid;
   if (tail == 0) return 0;
   const long long work = static_cast<long long>(tail) * p.k_iters;
-  const long long ctas = std::min<long long>(grid, work / kMinSplitIters);
+  const long long ctas = std::min<long long>(grid, work / min_iters);
   if (ctas <= tail) return 0;   // each CTA would still get whole tiles
   int max_seg = 1;
   for (long i = 0; i < tail; ++i) {
@@ -422,20 +423,24 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n, bool a_mn_major,
 }
 
 // ---------------------------------------------------------------- TF32 split
-// Nearest TF32 value of an fp32 bit pattern (10 explicit mantissa bits),
-// ties away from zero: add half of the 13 dropped bits to the magnitude and
-// clear them.  A carry into the exponent is the correct round-up.  Finite
-// inputs below 2^128 * (1 - 2^-12) only; larger ones round to infinity.
+// The tensor core reads a 32-bit operand as TF32 by dropping its 13 low
+// mantissa bits (measured on GB300 for both shared-memory and tensor-memory
+// operands).  The helpers below therefore leave those bits as they are and
+// only arrange that dropping them gives the intended TF32 value.
+
+// Bits that the tensor core reads as the nearest TF32 value of x (10
+// explicit mantissa bits), ties away from zero: half of the 13 dropped bits is
+// added to the magnitude, and the truncation on read completes the rounding.
+// A carry into the exponent is the correct round-up.  Finite inputs below
+// 2^128 * (1 - 2^-12) only; larger ones round to infinity.
 __device__ __forceinline__ uint32_t tf32_round_bits(uint32_t x) {
-  return (x + 0x1000u) & 0xFFFFE000u;
+  return x + 0x1000u;
 }
 
-// Low part for an operand whose high part is the raw fp32 value: the tensor
-// core reads a 32-bit operand as TF32 by dropping its 13 low mantissa bits
-// (measured on GB300 for both shared-memory and tensor-memory operands), so
-// the high part it sees is trunc(x) = x with those bits cleared.  The rest,
-// x - trunc(x), is exact in fp32 and is rounded to the nearest TF32 value so
-// that the tensor core reads it unchanged.
+// Low part for an operand whose high part is the raw fp32 value: the high
+// part the tensor core sees is trunc(x), x with the 13 low bits cleared.  The
+// rest, x - trunc(x), is exact in fp32, and the returned bits make the tensor
+// core read it rounded to the nearest TF32 value.
 __device__ __forceinline__ uint32_t tf32_lo_of_truncated(uint32_t x) {
   const float r = __fsub_rn(__uint_as_float(x), __uint_as_float(x & 0xFFFFE000u));
   return tf32_round_bits(__float_as_uint(r));

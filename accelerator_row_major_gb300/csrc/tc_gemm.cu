@@ -594,6 +594,22 @@ int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const CUtensorMap& m
   }
 }
 
+// Tile heights 64 and 128 are also built with BK = 32 for three products:
+// fewer, larger stages (the MMA thread's wait on a stage costs about as much
+// as the stage's MMAs at these heights).
+template <int NPROD, bool TMA>
+int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const CUtensorMap& ma,
+                 const CUtensorMap& mb, int grid, cudaStream_t stream) {
+  if (NPROD == 1) return launch_tm<32, 1, TMA>(tm, g, p, ma, mb, grid, stream);
+  if (bk == 16) return launch_tm<16, 3, TMA>(tm, g, p, ma, mb, grid, stream);
+  return tm == 64 ? launch_one<64, 32, 3, TMA>(g, p, ma, mb, grid, stream)
+                  : launch_one<128, 32, 3, TMA>(g, p, ma, mb, grid, stream);
+}
+
+// K depth of a stage: 32 for one product; for three, 32 at tile heights
+// up to 128 and 16 at 256 (where 32 would leave room for two stages only).
+int bk_for(int nprod, int tm) { return (nprod == 1 || tm <= 128) ? 32 : 16; }
+
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Tile height TM.  With the split tail the schedule no longer quantises to
@@ -629,7 +645,7 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
 int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
   *launches = 0;
-  const int bk = nprod == 3 ? 16 : 32;
+  int bk = 0;
   TcParams p;
   p.A = g.A;
   p.B = g.B;
@@ -638,7 +654,6 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   p.N = g.N;
   p.K = g.K;
   p.tiles_n = ceil_div(g.N, kTN);
-  p.k_iters = ceil_div(g.K, bk);
   p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
   p.partials = nullptr;
@@ -653,6 +668,8 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   size_t ws_bytes = 0;
   if (!(g.flags & (GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K))) {
     tm = choose_tm(g, true);
+    bk = bk_for(nprod, tm);
+    p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
     const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
     if (tiles <= 0x7fffffffL)
@@ -663,6 +680,8 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (ws_bytes) ws = acquire_workspace(g.device, stream, ws_bytes, &must_clear);
   if (!ws) {
     tm = choose_tm(g, false);
+    bk = bk_for(nprod, tm);
+    p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
     p.sk_ctas = 0;
     p.sk_work = 0;
@@ -705,11 +724,11 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   }
   int rc;
   if (nprod == 3) {
-    rc = tma ? launch_tm<16, 3, true>(tm, g, p, ma, mb, grid, stream)
-             : launch_tm<16, 3, false>(tm, g, p, ma, mb, grid, stream);
+    rc = tma ? launch_tm_bk<3, true>(tm, bk, g, p, ma, mb, grid, stream)
+             : launch_tm_bk<3, false>(tm, bk, g, p, ma, mb, grid, stream);
   } else {
-    rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
-             : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
+    rc = tma ? launch_tm_bk<1, true>(tm, bk, g, p, ma, mb, grid, stream)
+             : launch_tm_bk<1, false>(tm, bk, g, p, ma, mb, grid, stream);
   }
   if (rc == GEMM_F32_OK) {
     *launches += 1;
@@ -750,7 +769,6 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
   });
   if (!fs.ptr) return GEMM_F32_EDEVICE;
 
-  const int bk = nprod == 3 ? 16 : 32;
   TcParams p;
   p.A = g.A;
   p.B = g.B;
@@ -759,12 +777,13 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
   p.N = g.N;
   p.K = g.K;
   p.tiles_n = ceil_div(g.N, kTN);
-  p.k_iters = ceil_div(g.K, bk);
   p.drop_first_copy = 0;
   p.err = g.err;
   p.partials = nullptr;
   p.counters = nullptr;
   int tm = choose_tm(g, true);
+  int bk = bk_for(nprod, tm);
+  p.k_iters = ceil_div(g.K, bk);
   p.tiles_m = ceil_div(g.M, tm);
   long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
@@ -785,6 +804,8 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
     *launches += 1;
   } else {
     tm = choose_tm(g, false);
+    bk = bk_for(nprod, tm);
+    p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
     tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
     if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
@@ -809,11 +830,11 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
   }
   int rc;
   if (nprod == 3) {
-    rc = tma ? launch_tm<16, 3, true>(tm, g, p, ma, mb, grid, stream)
-             : launch_tm<16, 3, false>(tm, g, p, ma, mb, grid, stream);
+    rc = tma ? launch_tm_bk<3, true>(tm, bk, g, p, ma, mb, grid, stream)
+             : launch_tm_bk<3, false>(tm, bk, g, p, ma, mb, grid, stream);
   } else {
-    rc = tma ? launch_tm<32, 1, true>(tm, g, p, ma, mb, grid, stream)
-             : launch_tm<32, 1, false>(tm, g, p, ma, mb, grid, stream);
+    rc = tma ? launch_tm_bk<1, true>(tm, bk, g, p, ma, mb, grid, stream)
+             : launch_tm_bk<1, false>(tm, bk, g, p, ma, mb, grid, stream);
   }
   if (rc == GEMM_F32_OK) {
     *launches += 1;
