@@ -67,6 +67,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_last_launches.restype = ci
     lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
     lib.gemm_f32_noalloc.restype = ci
+    lib.gemm_f32_ladder.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+    lib.gemm_f32_ladder.restype = ci
     lib.gemm_f32_last_kernel.argtypes = []
     lib.gemm_f32_last_kernel.restype = ctypes.c_char_p
     lib.gemm_f32_release.argtypes = []
@@ -129,6 +131,15 @@ def gemm_f32_noalloc(A, B, C, M: int, N: int, K: int, mode=MODE_TC3X, stream=Non
     if isinstance(mode, str):
         mode = MODES[mode]
     return lib().gemm_f32_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(mode), _stream(stream))
+
+
+LADDER_STEPS = (0, 1, 2, 3, 4)
+
+
+def gemm_f32_ladder(A, B, C, M: int, N: int, K: int, step: int, stream=None) -> int:
+    """C = A * B with the pages' teaching kernel v<step> (0 .. 4); see
+    include/gemm_f32.h.  Not the product path."""
+    return lib().gemm_f32_ladder(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(step), _stream(stream))
 
 
 def gemm_f32_status(stream=None):

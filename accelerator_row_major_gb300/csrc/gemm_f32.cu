@@ -135,6 +135,39 @@ void* gemm_f32_impl::acquire_workspace(int device, cudaStream_t stream, size_t b
   return w.ptr;
 }
 
+namespace {
+
+// Checks of the operands shared by the entry points, before any CUDA call:
+// GEMM_F32_EINVAL, or 1 when there is nothing to compute (M or N zero), or 0.
+int check_operands(const float* A, const float* B, const float* C, int M, int N, int K) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_F32_EINVAL;
+  if (M == 0 || N == 0) return 1;
+  const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+  const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * sizeof(float);
+  const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * sizeof(float);
+  if (C == nullptr) return GEMM_F32_EINVAL;
+  if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_F32_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 3u)
+    return GEMM_F32_EINVAL;
+  if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return GEMM_F32_EINVAL;
+  return 0;
+}
+
+// K == 0: an empty sum, C = 0.
+int zero_fill(float* C, int M, int N, cudaStream_t stream) {
+  const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
+  if (cudaMemsetAsync(C, 0, c_bytes, stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
+  t_last_launches = 1;
+  t_last_kernel = "memset";
+  return GEMM_F32_OK;
+}
+
+}  // namespace
+
 extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
                            unsigned flags, gemm_f32_stream_t stream_handle) {
   t_last_launches = 0;
@@ -147,31 +180,15 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
   const unsigned bn_flags = flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256);
   if (bn_flags & (bn_flags - 1)) return GEMM_F32_EINVAL;  // at most one tile width
   if ((flags & GEMM_F32_FLAG_CTA_PAIR) && (flags & GEMM_F32_FLAG_SINGLE_CTA)) return GEMM_F32_EINVAL;
-  if (M == 0 || N == 0) return GEMM_F32_OK;
-  const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
-  const size_t a_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * sizeof(float);
-  const size_t b_bytes = static_cast<size_t>(K) * static_cast<size_t>(N) * sizeof(float);
-  if (C == nullptr) return GEMM_F32_EINVAL;
-  if (K > 0 && (A == nullptr || B == nullptr)) return GEMM_F32_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
-       reinterpret_cast<uintptr_t>(C)) & 3u)
-    return GEMM_F32_EINVAL;
-  if (overlaps(C, c_bytes, A, a_bytes) || overlaps(C, c_bytes, B, b_bytes)) return GEMM_F32_EINVAL;
+  const int chk = check_operands(A, B, C, M, N, K);
+  if (chk != 0) return chk < 0 ? chk : GEMM_F32_OK;
 
   int dev = 0;
   DeviceState* st = device_state(&dev);
   if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
 
-  if (K == 0) {  // an empty sum: C = 0
-    if (cudaMemsetAsync(C, 0, c_bytes, stream) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return GEMM_F32_ELAUNCH;
-    }
-    t_last_launches = 1;
-    t_last_kernel = "memset";
-    return GEMM_F32_OK;
-  }
+  if (K == 0) return zero_fill(C, M, N, stream);
 
   gemm_f32_impl::GemmArgs g;
   g.A = A;
@@ -200,6 +217,38 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
 extern "C" int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K,
                         gemm_f32_stream_t stream) {
   return gemm_f32_ex(A, B, C, M, N, K, default_mode(), 0u, stream);
+}
+
+extern "C" int gemm_f32_ladder(const float* A, const float* B, float* C, int M, int N, int K,
+                               int step, gemm_f32_stream_t stream_handle) {
+  t_last_launches = 0;
+  t_last_kernel = "none";
+  if (step < 0 || step > 4) return GEMM_F32_EINVAL;
+  const int chk = check_operands(A, B, C, M, N, K);
+  if (chk != 0) return chk < 0 ? chk : GEMM_F32_OK;
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  if (K == 0) return zero_fill(C, M, N, stream);
+  gemm_f32_impl::GemmArgs g;
+  g.A = A;
+  g.B = B;
+  g.C = C;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.err = st->err;
+  g.num_sms = st->num_sms;
+  g.device = dev;
+  g.flags = 0;
+  int launches = 0;
+  const int rc = gemm_f32_impl::launch_ladder(g, step, stream, &launches);
+  if (rc == GEMM_F32_OK) {
+    t_last_launches = launches;
+    t_last_kernel = g.kernel;
+  }
+  return rc;
 }
 
 extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,

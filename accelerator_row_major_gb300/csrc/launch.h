@@ -44,4 +44,7 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
 // CUDA-core FFMA path.
 int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches);
 
+// The pages' ladder kernels v0 .. v4 (step), for timing and teaching.
+int launch_ladder(GemmArgs& g, int step, cudaStream_t stream, int* launches);
+
 }  // namespace gemm_f32_impl

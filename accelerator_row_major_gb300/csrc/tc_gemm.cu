@@ -427,30 +427,49 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < KH; ++k) split_operand<NPROD>(braw[(kh0 + k) * kTN + col], bh[k], bl[k]);
         } else {
           const int m0 = c.tm * TM, n0 = c.tn * kTN, k0 = kt * BK;
-          // A tile: row r, column k; lanes run along k (coalesced)
-#pragma unroll 2
-          for (int e = tt; e < TM * BK; e += kTransformThreads) {
-            const int r = e / BK, k = e % BK;
-            const int gm = m0 + r, gk = k0 + k;
-            const uint32_t x = (gm < p.M && gk < p.K)
-                                   ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
-                                   : 0u;
-            uint32_t h, l;
-            split_operand<NPROD>(x, h, l);
-            const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
-            *reinterpret_cast<uint32_t*>(st + o) = h;
-            if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
-          }
-          // B tile: column n0 + col, K rows of this thread's half (lanes along n: coalesced)
+          // This thread's loads for the stage are issued before any of them
+          // is used (A in chunks of at most 16, the first with all of B), so
+          // a few latencies cover the stage.
+          constexpr int AV = TM * BK / kTransformThreads;   // A elements per thread
+          constexpr int CH = AV <= 16 ? AV : (KH >= 16 ? 8 : 16);   // within 128 registers
+          uint32_t bv[KH];
           const int gn = n0 + col;
 #pragma unroll
-          for (int k = 0; k < KH; ++k) {
-            const int gk = k0 + kh0 + k;
-            const uint32_t x = (gn < p.N && gk < p.K)
-                                   ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
-                                   : 0u;
-            split_operand<NPROD>(x, bh[k], bl[k]);
+          for (int c0 = 0; c0 < AV; c0 += CH) {
+            uint32_t av[CH];
+            // A tile: element e = tt + 256 j is row e / BK, column e % BK
+            // (lanes run along k: coalesced)
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int e = tt + (c0 + j) * kTransformThreads;
+              const int gm = m0 + e / BK, gk = k0 + e % BK;
+              av[j] = (gm < p.M && gk < p.K)
+                          ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
+                          : 0u;
+            }
+            if (c0 == 0) {
+              // B tile: column n0 + col, K rows of this thread's half (lanes along n)
+#pragma unroll
+              for (int k = 0; k < KH; ++k) {
+                const int gk = k0 + kh0 + k;
+                bv[k] = (gn < p.N && gk < p.K)
+                            ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
+                            : 0u;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int e = tt + (c0 + j) * kTransformThreads;
+              uint32_t h, l;
+              split_operand<NPROD>(av[j], h, l);
+              const uint32_t o = swizzle(static_cast<uint32_t>((e / BK) * BK * 4 + (e % BK) * 4),
+                                         Cfg::A_SWZ_MASK);
+              *reinterpret_cast<uint32_t*>(st + o) = h;
+              if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+            }
           }
+#pragma unroll
+          for (int k = 0; k < KH; ++k) split_operand<NPROD>(bv[k], bh[k], bl[k]);
         }
         const uint32_t bt =
             lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS + kh0);

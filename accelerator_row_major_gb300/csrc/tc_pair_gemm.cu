@@ -552,28 +552,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int m0 = c.tm * kPairTile + static_cast<int>(rank) * kHalf;
           const int n0 = c.tn * kPairTile + static_cast<int>(rank) * kHalf;
           const int k0 = kt * BK;
-#pragma unroll 2
-          for (int e = tt; e < kHalf * BK; e += kTransformWarps * 32) {
-            const int r = e / BK, k = e % BK;
-            const int gm = m0 + r, gk = k0 + k;
-            const uint32_t x = (gm < p.M && gk < p.K)
-                                   ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
-                                   : 0u;
-            uint32_t h, l;
-            split_operand<NPROD>(x, h, l);
-            const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
-            *reinterpret_cast<uint32_t*>(st + o) = h;
-            if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+          // All of this thread's loads for the stage are issued before any
+          // of them is used, so one latency covers the stage.
+          constexpr int AV = kHalf * BK / (kTransformWarps * 32);   // 8 or 16
+          uint32_t av[AV], bv[KH];
+#pragma unroll
+          for (int j = 0; j < AV; ++j) {
+            // element e = tt + 256 j: row e / BK, column e % BK (lanes along k)
+            const int e = tt + j * kTransformWarps * 32;
+            const int gm = m0 + e / BK, gk = k0 + e % BK;
+            av[j] = (gm < p.M && gk < p.K)
+                        ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
+                        : 0u;
           }
           const int gn = n0 + col;
 #pragma unroll
           for (int k = 0; k < KH; ++k) {
             const int gk = k0 + kh0 + k;
-            const uint32_t x = (gn < p.N && gk < p.K)
-                                   ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
-                                   : 0u;
-            split_operand<NPROD>(x, bh[k], bl[k]);
+            bv[k] = (gn < p.N && gk < p.K)
+                        ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
+                        : 0u;
           }
+#pragma unroll
+          for (int j = 0; j < AV; ++j) {
+            const int e = tt + j * kTransformWarps * 32;
+            uint32_t h, l;
+            split_operand<NPROD>(av[j], h, l);
+            const uint32_t o = swizzle(static_cast<uint32_t>((e / BK) * BK * 4 + (e % BK) * 4),
+                                       Cfg::A_SWZ_MASK);
+            *reinterpret_cast<uint32_t*>(st + o) = h;
+            if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+          }
+#pragma unroll
+          for (int k = 0; k < KH; ++k) split_operand<NPROD>(bv[k], bh[k], bl[k]);
         }
         const uint32_t bt =
             lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS + kh0);

@@ -60,6 +60,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--ladder", action="store_true",
+                    help="instead of the one-line benchmark: time the pages' kernels v0..v4, this "
+                         "library's modes and torch.matmul on the pages' two sizes (one JSON line per "
+                         "row, then a table on stderr)")
     return ap.parse_args(argv)
 
 
@@ -397,8 +401,99 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------- the pages' ladder
+def time_calls(fn, stream, warmup: int, reps: int, batches: int = 5):
+    """Mean device time per call (ms) of `batches` batches of `reps` calls of
+    fn() on `stream`, each batch bracketed by CUDA events; warm L2 as on the
+    pages (the same inputs every call)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+    torch.cuda.synchronize()
+    means = []
+    for _ in range(batches):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        means.append(e0.elapsed_time(e1) / reps)
+    return means
+
+
+def run_ladder(args):
+    """The pages' benchmark table ("LeetGPU problem 2: matrix multiplication",
+    yekq.top, section "benchmark summary": each version warmed up once, then
+    the mean of 10 runs, GFLOPS = 2MNK/t, % of cuBLAS) re-measured on this
+    GPU: the pages' kernels v0..v4 (gemm_f32_ladder), this library's three
+    modes (gemm_f32_ex) and, as context, torch.matmul (cuBLAS) in fp32 and
+    with TF32 allowed.  Reported: the mean over batches of `--steps` calls
+    (at least 10, the pages' count) and the median of the batch means."""
+    import torch
+
+    import accelerator_row_major_gb300 as g
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    rows = []
+    for cfg in ("c2", "c3"):
+        p = workloads.CONFIGS[cfg]
+        A_h, B_h = workloads.problem_inputs(cfg)
+        A = torch.from_numpy(A_h).to(dev)
+        B = torch.from_numpy(B_h).to(dev)
+        C = torch.empty((p.M, p.N), dtype=torch.float32, device=dev)
+        flop = workloads.gemm_flops(p.M, p.N, p.K)
+        cands = []
+        for step in g.LADDER_STEPS:
+            cands.append(("v%d" % step, "ladder_v%d" % step,
+                          lambda step=step: g.check(g.gemm_f32_ladder(A, B, C, p.M, p.N, p.K, step, stream))))
+        for mode in ("ffma", "tc3x", "tc1x"):
+            cands.append((mode, None,
+                          lambda mode=mode: g.check(g.gemm_f32_ex(A, B, C, p.M, p.N, p.K, mode, 0, stream))))
+
+        def torch_mm(tf32):
+            def fn():
+                torch.backends.cuda.matmul.allow_tf32 = tf32
+                torch.matmul(A, B, out=C)
+            return fn
+        cands.append(("torch.matmul fp32", "cuBLAS (context)", torch_mm(False)))
+        cands.append(("torch.matmul tf32", "cuBLAS (context)", torch_mm(True)))
+        results = []
+        for name, kernel, fn in cands:
+            times = time_calls(fn, stream, max(args.warmup, 3), max(args.steps, 10))   # batch means
+            if kernel is None:
+                kernel = g.gemm_f32_last_kernel()
+            mean = statistics.fmean(times)
+            results.append((name, kernel, mean, statistics.median(times)))
+        torch.backends.cuda.matmul.allow_tf32 = False
+        ref = next(r for r in results if r[0] == "torch.matmul fp32")[2]
+        for name, kernel, mean, med in results:
+            row = {"config": cfg, "shape": [p.M, p.K, p.N], "version": name, "kernel": kernel,
+                   "mean_ms": round(mean, 5), "median_ms": round(med, 5),
+                   "gflops_mean": round(flop / mean / 1e6, 1), "gflops_median": round(flop / med / 1e6, 1),
+                   "pct_of_cublas_fp32": round(100.0 * ref / mean, 1),
+                   "stat": "warm L2; %d warm-up calls, then 5 batches of %d calls, each batch timed "
+                           "with CUDA events" % (max(args.warmup, 3), max(args.steps, 10))}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+    sys.stderr.write("\n| size | version | kernel | mean ms | GFLOPS | % of torch fp32 |\n|---|---|---|---|---|---|\n")
+    for r in rows:
+        sys.stderr.write("| %s | %s | %s | %.4f | %.0f | %.1f |\n" % (
+            "x".join(str(v) for v in r["shape"]), r["version"], r["kernel"], r["mean_ms"],
+            r["gflops_mean"], r["pct_of_cublas_fp32"]))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.ladder:
+        return run_ladder(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

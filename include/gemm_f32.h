@@ -127,7 +127,8 @@ int gemm_f32_last_launches(void);
 /* Name of the kernel the last successful call on this host thread launched:
  * "tc_pair_kernel" (tensor cores, 256 x 256 tiles on SM pairs),
  * "tc_gemm_kernel" (tensor cores, one SM per tile), "ffma_gemm_kernel",
- * "memset" (K == 0) or "none" (nothing launched).  Static string. */
+ * "memset" (K == 0), "ladder_v0" .. "ladder_v4" (gemm_f32_ladder) or
+ * "none" (nothing launched).  Static string. */
 const char* gemm_f32_last_kernel(void);
 
 /* Frees the current device's workspaces after synchronising the device.
@@ -161,6 +162,23 @@ int gemm_f32_release(void);
  * The result equals gemm_f32_ex's for the same mode. */
 int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                      int mode, gemm_f32_stream_t stream);
+
+/* The pages' optimisation ladder for this GEMM ("LeetGPU problem 2: matrix
+ * multiplication", yekq.top, sections v0 .. v4 and "benchmark summary"),
+ * rebuilt for sm_103a so that each step can be timed on this GPU.  Teaching
+ * kernels, not the product path: C = A * B in fp32 fused multiply-adds
+ * (ascending k, bound 1e-5 * (|A||B|)_ij as GEMM_F32_MODE_FFMA) by
+ *   step 0  one thread per output, threadIdx.x along the rows of C;
+ *   step 1  one thread per output, threadIdx.x along the columns;
+ *   step 2  16 x 16 shared-memory tiles, zero-filled at the edges;
+ *   step 3  64 x 64 block tiles, 4 outputs of one row per thread;
+ *   step 4  64 x 64 block tiles, 4 x 4 outputs per thread.
+ * Arguments, layout, ownership and errors as gemm_f32_ex; GEMM_F32_EINVAL
+ * also for a step outside 0 .. 4 or a grid beyond the launch limits (more
+ * than 65535 blocks along y: N > 1048560 for step 0, M > 1048560 for steps 1
+ * and 2, M > 4194240 for steps 3 and 4).  Allocates nothing. */
+int gemm_f32_ladder(const float* A, const float* B, float* C, int M, int N, int K, int step,
+                    gemm_f32_stream_t stream);
 
 /* Static version string, e.g. "gemm_f32 1.0 sm_103a". */
 const char* gemm_f32_version(void);

@@ -20,12 +20,13 @@ def lib():
 
 
 def run_abi(A: np.ndarray, B: np.ndarray, mode="tc3x", flags=0, offset_a=0, offset_b=0,
-            offset_c=0, repeats=1, stream=None):
-    """C = A @ B through gemm_f32_ex on cuda:0.
+            offset_c=0, repeats=1, stream=None, ladder_step=None):
+    """C = A @ B through gemm_f32_ex on cuda:0 (through gemm_f32_ladder with
+    that step when ladder_step is given).
 
     offset_*: extra floats before each operand (4 bytes each), to move the
     base pointers off 16-byte alignment.  C sits inside a sentinel-filled
-    buffer; returns (C, guards_intact, results of every repeat)."""
+    buffer; returns (C, results of every repeat)."""
     import torch
 
     g = lib()
@@ -44,8 +45,11 @@ def run_abi(A: np.ndarray, B: np.ndarray, mode="tc3x", flags=0, offset_a=0, offs
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     outs = []
     for _ in range(repeats):
-        rc = g.gemm_f32_ex(a_ptr, b_ptr, c_ptr, M, N, K, mode, flags, s)
-        assert rc == g.GEMM_F32_OK, "gemm_f32_ex returned %d" % rc
+        if ladder_step is None:
+            rc = g.gemm_f32_ex(a_ptr, b_ptr, c_ptr, M, N, K, mode, flags, s)
+        else:
+            rc = g.gemm_f32_ladder(a_ptr, b_ptr, c_ptr, M, N, K, ladder_step, s)
+        assert rc == g.GEMM_F32_OK, "the call returned %d" % rc
         expect = (0,) if (M == 0 or N == 0) else (1, 2)
         assert g.gemm_f32_last_launches() in expect
         st, site = g.gemm_f32_status(s)

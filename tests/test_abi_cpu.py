@@ -21,7 +21,7 @@ def g():
 
 def test_header_declares_the_entry_points(g):
     names = g.declared_symbols()
-    assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status",
+    assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status", "gemm_f32_ladder",
                             "gemm_f32_last_kernel", "gemm_f32_last_launches", "gemm_f32_noalloc",
                             "gemm_f32_release",
                             "gemm_f32_version"])
@@ -64,6 +64,18 @@ def test_malformed_requests_are_rejected_on_the_host(g, args, mode, flags):
     assert g.gemm_f32_last_launches() == 0
 
 
+@pytest.mark.parametrize("args,step", [
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, 4), -1),             # step below 0
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, 4), 5),              # step above 4
+    ((FAKE_A, FAKE_B, FAKE_C, -1, 4, 4), 0),             # negative M
+    ((FAKE_A, FAKE_B, 0, 4, 4, 4), 3),                   # null C
+    ((FAKE_A, FAKE_B, FAKE_A + 8, 4, 4, 4), 4),          # C overlaps A
+])
+def test_ladder_rejects_malformed_requests_on_the_host(g, args, step):
+    assert g.gemm_f32_ladder(*args, step=step) == g.GEMM_F32_EINVAL
+    assert g.gemm_f32_last_launches() == 0
+
+
 def test_empty_outputs_are_a_no_op(g):
     # M == 0 or N == 0: nothing to write, no CUDA call, success
     assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 0, 5, 5) == g.GEMM_F32_OK
@@ -71,6 +83,9 @@ def test_empty_outputs_are_a_no_op(g):
     assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 5, 0, 5) == g.GEMM_F32_OK
     assert g.gemm_f32_ex(0, 0, 0, 0, 0, 0) == g.GEMM_F32_OK
     assert g.gemm_f32_last_launches() == 0
+    for step in range(5):
+        assert g.gemm_f32_ladder(FAKE_A, FAKE_B, FAKE_C, 0, 5, 5, step) == g.GEMM_F32_OK
+    assert g.gemm_f32_last_kernel() == "none"
 
 
 def test_no_gpu_is_reported_as_unsupported_device(g):
