@@ -14,7 +14,8 @@ the tolerance of every parity check.
 
 Two implementations of the same formula live here:
   * ``gemm`` / ``gemm_entries``: plain C (``gemm_oracle.c``), OpenMP over
-    rows, compiled with ``-ffp-contract=off``;
+    rows, compiled with ``-ffp-contract=off``; ``gemm_general`` adds the
+    scaled, strided and transposed form C = alpha op(A) op(B) + beta C;
   * ``gemm_py``: pure-Python loops, for tiny cases only.
 Both are pinned by the ``-m "not gpu"`` tests against closed forms, brute
 force with exact rational arithmetic, invariants and the pages' printed
@@ -60,6 +61,10 @@ def _load():
             lib.oracle_gemm_entries.argtypes = [ptr, ptr, i64, i64, i64, ptr, ptr, i64,
                                                 ptr, ptr, ctypes.c_int]
             lib.oracle_gemm_entries.restype = ctypes.c_int
+            f32 = ctypes.c_float
+            lib.oracle_gemm_general.argtypes = [ctypes.c_int, ctypes.c_int, i64, i64, i64, f32, ptr, i64,
+                                                ptr, i64, f32, ptr, i64, ptr, ctypes.c_int]
+            lib.oracle_gemm_general.restype = ctypes.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -117,6 +122,37 @@ def gemm_entries(A, B, rows, cols, threads: int = 0):
     if rc != 0:
         raise RuntimeError("oracle_gemm_entries failed (%d)" % rc)
     return out, out_abs
+
+
+def gemm_general(A, B, C, M: int, N: int, K: int, alpha: float = 1.0, beta: float = 0.0,
+                 trans_a: bool = False, trans_b: bool = False, threads: int = 0):
+    """C = alpha * op(A) * op(B) + beta * C on row-major storage arrays.
+
+    A, B, C are 2-D float32 arrays holding the stored matrices; each one's
+    row stride is its width (so a wider array is a padded leading
+    dimension).  With trans_a, A stores op(A)^T (K x M window); with
+    trans_b, B stores op(B)^T (N x K window).  Only C[:M, :N] changes.
+    Returns (new C, a copy; absC float64 [M, N] = |alpha| |op(A)||op(B)| +
+    |beta| |C_old|)."""
+    A = _as_f32(A)
+    B = _as_f32(B)
+    C = _as_f32(C).copy()
+    for name, x in (("A", A), ("B", B), ("C", C)):
+        if x.ndim != 2:
+            raise ValueError("%s must be 2-D" % name)
+    ra, ca = (K, M) if trans_a else (M, K)
+    rb, cb = (N, K) if trans_b else (K, N)
+    if A.shape[0] < ra or A.shape[1] < ca or B.shape[0] < rb or B.shape[1] < cb \
+            or C.shape[0] < M or C.shape[1] < N:
+        raise ValueError("stored arrays smaller than the windows")
+    absC = np.empty((M, N), np.float64)
+    rc = _load().oracle_gemm_general(int(bool(trans_a)), int(bool(trans_b)), M, N, K, float(alpha),
+                                     A.ctypes.data, A.shape[1], B.ctypes.data, B.shape[1],
+                                     float(beta), C.ctypes.data, C.shape[1], absC.ctypes.data,
+                                     int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle_gemm_general failed (%d)" % rc)
+    return C, absC
 
 
 def gemm_py(A, B):

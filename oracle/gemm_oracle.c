@@ -112,6 +112,57 @@ int oracle_gemm_entries(const float* A, const float* B, int64_t M, int64_t N, in
     return 0;
 }
 
+/* General form (row-major storage throughout):
+ *   C = alpha * op(A) * op(B) + beta * C
+ * where op(A) is M x K and is either A, stored M x K with row stride lda
+ * (trans_a == 0), or the transpose of A stored K x M with row stride lda
+ * (trans_a == 1); likewise op(B) is K x N, either B stored K x N or the
+ * transpose of B stored N x K, with row stride ldb; C is stored M x N with
+ * row stride ldc, and only that M x N window is read or written.  This is
+ * the scaled, strided, optionally transposed product of the cuBLAS call
+ * shown on "LeetGPU problem 2: matrix multiplication" (yekq.top, section
+ * "cuBLAS reference"), restated for row-major storage.
+ *
+ * The sum over k is formed exactly as in oracle_gemm_f64acc (exact products,
+ * double, ascending k from +0.0); then alpha * sum + beta * C_old is formed in
+ * double and rounded once to float.  When beta == 0, C_old is not read, so
+ * whatever C held (NaN included) does not matter (the BLAS convention).
+ * absC (dense M x N, may be NULL) receives |alpha| * sum_k |op(A)_ik| |op(B)_kj|
+ * + |beta| * |C_old_ij|, which scales the tolerance.  Returns 0 or -1. */
+int oracle_gemm_general(int trans_a, int trans_b, int64_t M, int64_t N, int64_t K, float alpha,
+                        const float* A, int64_t lda, const float* B, int64_t ldb, float beta,
+                        float* C, int64_t ldc, double* absC, int nthreads) {
+    if (M < 0 || N < 0 || K < 0) return -1;
+    if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return -1;
+    if (lda < (trans_a ? M : K) || ldb < (trans_b ? K : N) || ldc < N) return -1;
+    if (M == 0 || N == 0) return 0;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for num_threads(nthreads) schedule(dynamic, 1)
+#endif
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0, acc_abs = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const double a = (double)(trans_a ? A[k * lda + i] : A[i * lda + k]);
+                const double b = (double)(trans_b ? B[j * ldb + k] : B[k * ldb + j]);
+                acc += a * b;
+                acc_abs += fabs(a) * fabs(b);
+            }
+            double r = (double)alpha * acc;
+            double r_abs = fabs((double)alpha) * acc_abs;
+            if (beta != 0.0f) {
+                const double c = (double)C[i * ldc + j];
+                r += (double)beta * c;
+                r_abs += fabs((double)beta) * fabs(c);
+            }
+            C[i * ldc + j] = (float)r;
+            if (absC) absC[i * N + j] = r_abs;
+        }
+    }
+    return 0;
+}
+
 /* Number of threads an OpenMP region would use (for reporting). */
 int oracle_max_threads(void) {
 #ifdef _OPENMP
