@@ -67,6 +67,9 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_last_launches.restype = ci
     lib.gemm_f32_noalloc.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
     lib.gemm_f32_noalloc.restype = ci
+    cf = ctypes.c_float
+    lib.gemm_f32_general.argtypes = [ci, ci, ci, ci, ci, cf, vp, ci, vp, ci, cf, vp, ci, ci, vp]
+    lib.gemm_f32_general.restype = ci
     lib.gemm_f32_ladder.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
     lib.gemm_f32_ladder.restype = ci
     lib.gemm_f32_last_kernel.argtypes = []
@@ -131,6 +134,17 @@ def gemm_f32_noalloc(A, B, C, M: int, N: int, K: int, mode=MODE_TC3X, stream=Non
     if isinstance(mode, str):
         mode = MODES[mode]
     return lib().gemm_f32_noalloc(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(mode), _stream(stream))
+
+
+def gemm_f32_general(trans_a: int, trans_b: int, M: int, N: int, K: int, alpha: float, A, lda: int,
+                     B, ldb: int, beta: float, C, ldc: int, mode=MODE_TC3X, stream=None) -> int:
+    """C = alpha * op(A) * op(B) + beta * C on row-major storage with row
+    strides lda, ldb, ldc; trans_a / trans_b select stored transposes (see
+    include/gemm_f32.h)."""
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return lib().gemm_f32_general(int(trans_a), int(trans_b), M, N, K, float(alpha), _ptr(A), lda,
+                                  _ptr(B), ldb, float(beta), _ptr(C), ldc, int(mode), _stream(stream))
 
 
 LADDER_STEPS = (0, 1, 2, 3, 4)

@@ -66,6 +66,15 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n,
 // bumps the tile's counter; the CTA that bumps it last adds the partials in
 // segment order (fixed: the sum does not depend on which CTA is last).
 constexpr int kMinSplitIters = 64;       // least K iterations per CTA in the split tail
+
+// Operand loaders of the tensor-core kernels (a template parameter):
+// per-thread loads of the plain product, TMA tiles, or per-thread loads of
+// the general form (row strides, stored transposes).  The plain product's
+// staged kernel keeps its own code: the general form's indexing costs it
+// registers (measured on GB300: 88 -> 122 at TM = 64, 8 % slower).
+constexpr int kLoadStaged = 0;
+constexpr int kLoadTma = 1;
+constexpr int kLoadStagedGeneral = 2;
 constexpr size_t kCounterBytes = 4096;   // tile counters at the start of the workspace
 
 // One unit of a CTA's work: K iterations [k0, k1) of one output tile.
@@ -202,6 +211,59 @@ __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, in
 #pragma unroll
         for (int q = 0; q < 4; ++q)
           if (n + q < N) dst[q] = v[q];
+      }
+    }
+  }
+}
+
+// The same for the general form: row stride ldc and, with `scale`,
+// C = alpha * sum + beta * C_old (C_old read only when beta != 0).
+template <int ROWS, int COLS, int NTHREADS, int CHUNK>
+__device__ __forceinline__ void reduce_partials_general(const float* parts, int nseg, int m0,
+                                                        int n0, int M, int N, float* C, int ldc,
+                                                        int scale, float alpha, float beta) {
+  constexpr int kVec = ROWS * COLS / 4;            // float4s per partial
+  constexpr int kPer = kVec / NTHREADS;            // per thread
+  constexpr int kChunk = kPer < CHUNK ? kPer : CHUNK;
+  static_assert(kVec % NTHREADS == 0 && kPer % kChunk == 0, "partial tile shape");
+  const float4* const p4 = reinterpret_cast<const float4*>(parts);
+#pragma unroll 1
+  for (int base = 0; base < kPer; base += kChunk) {
+    float4 sum[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int sg = 0; sg < nseg; ++sg) {
+      float4 x[kChunk];
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i)
+        x[i] = __ldcg(p4 + static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS);
+#pragma unroll
+      for (int i = 0; i < kChunk; ++i) {
+        sum[i].x += x[i].x;
+        sum[i].y += x[i].y;
+        sum[i].z += x[i].z;
+        sum[i].w += x[i].w;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      const int f = threadIdx.x + (base + i) * NTHREADS;   // float4 index in the tile
+      const int m = m0 + f / (COLS / 4);
+      const int n = n0 + (f % (COLS / 4)) * 4;
+      if (m < M) {
+        float* dst = C + static_cast<size_t>(m) * static_cast<size_t>(ldc) + n;
+        const float v[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (n + q >= N) continue;
+          float r = v[q];
+          if (scale) {   // alpha * sum (+ beta * C_old when beta != 0)
+            r *= alpha;
+            if (beta != 0.0f) r = fmaf(beta, dst[q], r);
+          }
+          dst[q] = r;
+        }
       }
     }
   }

@@ -67,6 +67,18 @@ struct FfmaParams {
   unsigned* err;
 };
 
+// The general form's parameters: row strides, transposed storage (4-byte
+// copies only), alpha / beta (scale = 1), and whether rows of C take 16-byte
+// stores.  A separate kernel argument: measured on GB300, growing FfmaParams
+// changed the plain kernel's register allocation and cost it 2 %.
+struct FfmaGeneral {
+  int lda, ldb, ldc;
+  int trans_a, trans_b;
+  float alpha, beta;
+  int scale;
+  int c_vec;
+};
+
 // Two fused multiply-adds per lane: d.x = a.x * b.x + c.x, d.y = a.y * b.y + c.y
 // (each rounded once, as fmaf), on 64-bit register pairs.
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
@@ -107,13 +119,18 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 // Copies K tile `kt` of the block's A panel and B panel into one stage.
-// VEC: K % 4 == 0, N % 4 == 0 and 16-byte aligned A and B, so a 16-byte
-// chunk is either wholly inside the matrix or wholly outside.
-template <bool VEC>
-__device__ __forceinline__ void load_stage(const FfmaParams& p, int m0, int n0, int kt,
+// VEC: K % 4 == 0, N % 4 == 0, untransposed operands with row strides a
+// multiple of 4 and 16-byte aligned A and B, so a 16-byte chunk is either
+// wholly inside the matrix or wholly outside.  Otherwise 4-byte copies, which
+// also read transposed storage.
+template <bool VEC, bool GEN>
+__device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGeneral& gp, int m0,
+                                           int n0, int kt,
                                            uint32_t a_dst, uint32_t b_dst) {
   const int tid = threadIdx.x;
   const int k0 = kt * kBK;
+  const int lda = GEN ? gp.lda : p.K, ldb = GEN ? gp.ldb : p.N;
+  const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
   // A: 128 rows x 16 k = 512 chunks of 4 floats; thread -> chunks tid, tid + 256
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
@@ -123,14 +140,15 @@ __device__ __forceinline__ void load_stage(const FfmaParams& p, int m0, int n0, 
     const uint32_t dst = a_dst + (r * kAPitch + kc) * 4;
     if (VEC) {
       const bool in = gm < p.M && gk < p.K;
-      const float* src = in ? p.A + static_cast<size_t>(gm) * p.K + gk : p.A;
+      const float* src = in ? p.A + static_cast<size_t>(gm) * lda + gk : p.A;
       cp_async_16(dst, src, in ? 16u : 0u);
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const bool in = gm < p.M && gk + e < p.K;
-        const float* src = in ? p.A + static_cast<size_t>(gm) * p.K + gk + e : p.A;
-        cp_async_4(dst + 4 * e, src, in ? 4u : 0u);
+        const size_t at = trans_a ? static_cast<size_t>(gk + e) * lda + gm
+                                  : static_cast<size_t>(gm) * lda + gk + e;
+        cp_async_4(dst + 4 * e, in ? p.A + at : p.A, in ? 4u : 0u);
       }
     }
   }
@@ -143,21 +161,25 @@ __device__ __forceinline__ void load_stage(const FfmaParams& p, int m0, int n0, 
     const uint32_t dst = b_dst + (k * kBN + nc) * 4;
     if (VEC) {
       const bool in = gk < p.K && gn < p.N;
-      const float* src = in ? p.B + static_cast<size_t>(gk) * p.N + gn : p.B;
+      const float* src = in ? p.B + static_cast<size_t>(gk) * ldb + gn : p.B;
       cp_async_16(dst, src, in ? 16u : 0u);
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const bool in = gk < p.K && gn + e < p.N;
-        const float* src = in ? p.B + static_cast<size_t>(gk) * p.N + gn + e : p.B;
-        cp_async_4(dst + 4 * e, src, in ? 4u : 0u);
+        const size_t at = trans_b ? static_cast<size_t>(gn + e) * ldb + gk
+                                  : static_cast<size_t>(gk) * ldb + gn + e;
+        cp_async_4(dst + 4 * e, in ? p.B + at : p.B, in ? 4u : 0u);
       }
     }
   }
 }
 
-template <bool VEC>
-__global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams p) {
+// GEN: the general form (row strides, stored transposes, alpha / beta); a
+// separate instantiation, so that the plain product's code is unchanged.
+template <bool VEC, bool GEN>
+__global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams p,
+                                                                const FfmaGeneral gp) {
   extern __shared__ __align__(16) float smem_f[];
   __shared__ WorkItem pending[kMaxPending];   // split tiles this CTA must reduce
   __shared__ int pending_count;
@@ -186,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
       if (s < nk)
-        load_stage<VEC>(p, m0, n0, w.k0 + s, as_addr + s * kAStage * 4, bs_addr + s * kBStage * 4);
+        load_stage<VEC, GEN>(p, gp, m0, n0, w.k0 + s, as_addr + s * kAStage * 4,
+                             bs_addr + s * kBStage * 4);
       cp_async_commit();
     }
 
@@ -196,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
       const int nxt = j + kStages - 1;
       if (nxt < nk) {
         const int s = nxt % kStages;
-        load_stage<VEC>(p, m0, n0, w.k0 + nxt, as_addr + s * kAStage * 4,
-                        bs_addr + s * kBStage * 4);
+        load_stage<VEC, GEN>(p, gp, m0, n0, w.k0 + nxt, as_addr + s * kAStage * 4,
+                             bs_addr + s * kBStage * 4);
       }
       cp_async_commit();
 
@@ -234,23 +257,55 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
 
     if (w.nseg == 1) {
       // epilogue: rows ty + 16 i, columns 64 g + 4 tx .. +3
-      const bool c_vec = VEC && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
+      if constexpr (!GEN) {
+        const bool c_vec = VEC && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = m0 + ty + 16 * i;
-        if (r >= p.M) continue;
-        float* crow = p.C + static_cast<size_t>(r) * p.N;
+        for (int i = 0; i < 8; ++i) {
+          const int r = m0 + ty + 16 * i;
+          if (r >= p.M) continue;
+          float* crow = p.C + static_cast<size_t>(r) * p.N;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int n = n0 + g * 64 + tx * 4;
-          const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
-          const float v[4] = {lo.x, lo.y, hi.x, hi.y};
-          if (c_vec && n + 3 < p.N) {
-            *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
-          } else {
+          for (int g = 0; g < 4; ++g) {
+            const int n = n0 + g * 64 + tx * 4;
+            const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
+            const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+            if (c_vec && n + 3 < p.N) {
+              *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (n + q < p.N) crow[n + q] = v[q];
+              for (int q = 0; q < 4; ++q)
+                if (n + q < p.N) crow[n + q] = v[q];
+            }
+          }
+        }
+      } else {
+        // general form: row stride ldc; alpha * sum (+ beta * C_old, read
+        // only when beta != 0)
+        const bool c_vec = VEC && gp.c_vec != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = m0 + ty + 16 * i;
+          if (r >= p.M) continue;
+          float* crow = p.C + static_cast<size_t>(r) * gp.ldc;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int n = n0 + g * 64 + tx * 4;
+            const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
+            float v[4] = {lo.x, lo.y, hi.x, hi.y};
+            if (gp.scale) {
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                v[q] *= gp.alpha;
+                if (gp.beta != 0.0f && n + q < p.N) v[q] = fmaf(gp.beta, crow[n + q], v[q]);
+              }
+            }
+            if (c_vec && n + 3 < p.N) {
+              *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (n + q < p.N) crow[n + q] = v[q];
+            }
           }
         }
       }
@@ -288,9 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
     for (int e = 0; e < npend; ++e) {
       const WorkItem pw = pending[e];
       const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
-      reduce_partials<kBM, kBN, kThreads, 8>(
-          p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (kBM * kBN), pw.nseg,
-          c.tm * kBM, c.tn * kBN, p.M, p.N, p.C);
+      const float* parts = p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (kBM * kBN);
+      if constexpr (!GEN)
+        reduce_partials<kBM, kBN, kThreads, 8>(parts, pw.nseg, c.tm * kBM, c.tn * kBN, p.M, p.N,
+                                               p.C);
+      else
+        reduce_partials_general<kBM, kBN, kThreads, 8>(parts, pw.nseg, c.tm * kBM, c.tn * kBN,
+                                                       p.M, p.N, p.C, gp.ldc, gp.scale, gp.alpha,
+                                                       gp.beta);
       if (threadIdx.x == 0) p.counters[pw.tail] = 0;   // ready for the next call
     }
   }
@@ -298,19 +358,20 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
 
 constexpr int kMaxDevices = 64;
 
-template <bool VEC>
-int launch_vec(const GemmArgs& g, const FfmaParams& p, int grid, cudaStream_t stream) {
+template <bool VEC, bool GEN>
+int launch_vec(const GemmArgs& g, const FfmaParams& p, const FfmaGeneral& gp, int grid,
+               cudaStream_t stream) {
   static std::atomic<unsigned long long> configured{0};  // bit per device
   const unsigned long long bit = 1ull << (g.device % kMaxDevices);
   if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(ffma_gemm_kernel<VEC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes) != cudaSuccess) {
+    if (cudaFuncSetAttribute(ffma_gemm_kernel<VEC, GEN>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
       (void)cudaGetLastError();
       return GEMM_F32_ELAUNCH;
     }
     configured.fetch_or(bit);
   }
-  ffma_gemm_kernel<VEC><<<grid, kThreads, kSmemBytes, stream>>>(p);
+  ffma_gemm_kernel<VEC, GEN><<<grid, kThreads, kSmemBytes, stream>>>(p, gp);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;
 }
@@ -332,6 +393,16 @@ int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
   p.partials = nullptr;
   p.counters = nullptr;
   p.err = g.err;
+  FfmaGeneral gp;
+  gp.lda = g.lda;
+  gp.ldb = g.ldb;
+  gp.ldc = g.ldc;
+  gp.trans_a = g.trans_a;
+  gp.trans_b = g.trans_b;
+  gp.alpha = g.alpha;
+  gp.beta = g.beta;
+  gp.scale = g.scale;
+  gp.c_vec = g.ldc % 4 == 0 && reinterpret_cast<uintptr_t>(g.C) % 16 == 0;
   const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
   if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
   p.dp_tiles = static_cast<int>(tiles);
@@ -361,9 +432,16 @@ int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
       }
     }
   }
-  const bool vec = g.K % 4 == 0 && g.N % 4 == 0 && reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
-                   reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
-  const int rc = vec ? launch_vec<true>(g, p, grid, stream) : launch_vec<false>(g, p, grid, stream);
+  // 16-byte copies: untransposed, strides a multiple of 4 floats, aligned
+  // bases, and K, N multiples of 4 (a chunk is wholly inside or outside)
+  const bool vec = tma_addressable(g) && g.K % 4 == 0 && g.N % 4 == 0;
+  int rc;
+  if (!plain_form(g))
+    rc = vec ? launch_vec<true, true>(g, p, gp, grid, stream)
+             : launch_vec<false, true>(g, p, gp, grid, stream);
+  else
+    rc = vec ? launch_vec<true, false>(g, p, gp, grid, stream)
+             : launch_vec<false, false>(g, p, gp, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "ffma_gemm_kernel";

@@ -3,7 +3,9 @@
 // the contract of each entry point are documented in include/gemm_f32.h.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -154,6 +156,29 @@ int check_operands(const float* A, const float* B, const float* C, int M, int N,
   return 0;
 }
 
+// C = beta * C over an M x N window with row stride ldc (C = 0 when beta
+// is 0, without reading C).  The general form's case of an empty or
+// zero-weighted product.
+__global__ void scale_window_kernel(float* C, int M, int N, int ldc, float beta) {
+  const long long total = static_cast<long long>(M) * N;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    float* c = C + (t / N) * static_cast<long long>(ldc) + t % N;
+    *c = beta != 0.0f ? beta * *c : 0.0f;
+  }
+}
+
+int scale_window(float* C, int M, int N, int ldc, float beta, int num_sms, cudaStream_t stream) {
+  const long long total = static_cast<long long>(M) * N;
+  const long long want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < 4LL * num_sms ? want : 4LL * num_sms);
+  scale_window_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, beta);
+  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  t_last_launches = 1;
+  t_last_kernel = "scale_window_kernel";
+  return GEMM_F32_OK;
+}
+
 // K == 0: an empty sum, C = 0.
 int zero_fill(float* C, int M, int N, cudaStream_t stream) {
   const size_t c_bytes = static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float);
@@ -197,6 +222,9 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
   g.M = M;
   g.N = N;
   g.K = K;
+  g.lda = K;
+  g.ldb = N;
+  g.ldc = N;
   g.err = st->err;
   g.num_sms = st->num_sms;
   g.device = dev;
@@ -238,12 +266,84 @@ extern "C" int gemm_f32_ladder(const float* A, const float* B, float* C, int M, 
   g.M = M;
   g.N = N;
   g.K = K;
+  g.lda = K;
+  g.ldb = N;
+  g.ldc = N;
   g.err = st->err;
   g.num_sms = st->num_sms;
   g.device = dev;
   g.flags = 0;
   int launches = 0;
   const int rc = gemm_f32_impl::launch_ladder(g, step, stream, &launches);
+  if (rc == GEMM_F32_OK) {
+    t_last_launches = launches;
+    t_last_kernel = g.kernel;
+  }
+  return rc;
+}
+
+extern "C" int gemm_f32_general(int trans_a, int trans_b, int M, int N, int K, float alpha,
+                                const float* A, int lda, const float* B, int ldb, float beta,
+                                float* C, int ldc, int mode, gemm_f32_stream_t stream_handle) {
+  t_last_launches = 0;
+  t_last_kernel = "none";
+  // ---- host-only checks first
+  if ((trans_a != 0 && trans_a != 1) || (trans_b != 0 && trans_b != 1)) return GEMM_F32_EINVAL;
+  if (M < 0 || N < 0 || K < 0) return GEMM_F32_EINVAL;
+  if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_FFMA && mode != GEMM_F32_MODE_TC1X)
+    return GEMM_F32_EINVAL;
+  const int a_rows = trans_a ? K : M, a_cols = trans_a ? M : K;
+  const int b_rows = trans_b ? N : K, b_cols = trans_b ? K : N;
+  if (lda < std::max(1, a_cols) || ldb < std::max(1, b_cols) || ldc < std::max(1, N))
+    return GEMM_F32_EINVAL;
+  if (!std::isfinite(alpha) || !std::isfinite(beta)) return GEMM_F32_EINVAL;
+  if (M == 0 || N == 0) return GEMM_F32_OK;
+  const bool use_ab = K > 0 && alpha != 0.0f;
+  if (C == nullptr || (use_ab && (A == nullptr || B == nullptr))) return GEMM_F32_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(B) |
+       reinterpret_cast<uintptr_t>(C)) & 3u)
+    return GEMM_F32_EINVAL;
+  // byte extents of the stored windows (first to last element touched)
+  auto extent = [](int rows, int cols, int ld) -> size_t {
+    return rows > 0 && cols > 0
+               ? (static_cast<size_t>(rows - 1) * static_cast<size_t>(ld) + cols) * sizeof(float)
+               : 0;
+  };
+  const size_t c_bytes = extent(M, N, ldc);
+  if (use_ab && (overlaps(C, c_bytes, A, extent(a_rows, a_cols, lda)) ||
+                 overlaps(C, c_bytes, B, extent(b_rows, b_cols, ldb))))
+    return GEMM_F32_EINVAL;
+
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  if (!use_ab) return scale_window(C, M, N, ldc, beta, st->num_sms, stream);
+
+  gemm_f32_impl::GemmArgs g;
+  g.A = A;
+  g.B = B;
+  g.C = C;
+  g.M = M;
+  g.N = N;
+  g.K = K;
+  g.lda = lda;
+  g.ldb = ldb;
+  g.ldc = ldc;
+  g.trans_a = trans_a;
+  g.trans_b = trans_b;
+  g.alpha = alpha;
+  g.beta = beta;
+  g.scale = (alpha != 1.0f || beta != 0.0f) ? 1 : 0;
+  g.err = st->err;
+  g.num_sms = st->num_sms;
+  g.device = dev;
+  g.flags = 0;
+  int launches = 0;
+  const int rc = mode == GEMM_F32_MODE_FFMA
+                     ? gemm_f32_impl::launch_ffma(g, stream, &launches)
+                     : gemm_f32_impl::launch_tc(g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream,
+                                                &launches);
   if (rc == GEMM_F32_OK) {
     t_last_launches = launches;
     t_last_kernel = g.kernel;
@@ -288,6 +388,9 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
   g.M = M;
   g.N = N;
   g.K = K;
+  g.lda = K;
+  g.ldb = N;
+  g.ldc = N;
   g.err = st->err;
   g.num_sms = st->num_sms;
   g.device = dev;

@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstdint>
+
 namespace gemm_f32_impl {
 
 struct GemmArgs {
@@ -16,7 +18,28 @@ struct GemmArgs {
   int device;           // current device ordinal
   unsigned flags;       // GEMM_F32_FLAG_* bits
   const char* kernel = "none";   // set by the launcher: the kernel it launched
+  // General form C = alpha op(A) op(B) + beta C (row-major storage).  The
+  // plain product has lda = K, ldb = N, ldc = N, no transposes, alpha = 1,
+  // beta = 0 and scale = 0.
+  int lda = 0, ldb = 0, ldc = 0;   // row strides (elements) of the stored A, B, C
+  int trans_a = 0;                 // 1: A is stored K x M and op(A) = its transpose
+  int trans_b = 0;                 // 1: B is stored N x K and op(B) = its transpose
+  float alpha = 1.0f, beta = 0.0f;
+  int scale = 0;                   // 1 when alpha != 1 or beta != 0
 };
+
+// The plain product C = A * B on dense row-major storage (what gemm_f32 and
+// gemm_f32_ex compute): the kernels have separate code for it.
+inline bool plain_form(const GemmArgs& g) {
+  return !g.trans_a && !g.trans_b && g.lda == g.K && g.ldb == g.N && g.ldc == g.N && !g.scale;
+}
+
+// Whether the operands can be read by TMA tiles: untransposed, row strides a
+// multiple of 16 bytes, 16-byte aligned bases.
+inline bool tma_addressable(const GemmArgs& g) {
+  return !g.trans_a && !g.trans_b && g.lda % 4 == 0 && g.ldb % 4 == 0 &&
+         reinterpret_cast<uintptr_t>(g.A) % 16 == 0 && reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+}
 
 // The library's workspace for `stream` on `device` (one per device and
 // stream), grown to at least `bytes` with cudaMalloc when needed (which

@@ -92,6 +92,16 @@ struct TcParams {
   unsigned* err;
 };
 
+// The general form C = alpha op(A) op(B) + beta C: row strides, stored
+// transposes (staged loader only) and alpha / beta.  A separate kernel
+// argument, so that the plain product's parameters keep their layout.
+struct TcGeneral {
+  int lda, ldb, ldc;
+  int trans_a, trans_b;
+  float alpha, beta;
+  int scale;             // C = alpha * acc (+ beta * C when beta != 0)
+};
+
 template <int TM, int BK, int NPROD>
 struct TcCfg {
   static constexpr int A_BYTES = TM * BK * 4;                       // A hi (TMA target)
@@ -121,6 +131,13 @@ struct TcCfg {
 // which is how TMA writes and tcgen05 reads 64B / 128B swizzled tiles.
 __device__ __forceinline__ uint32_t swizzle(uint32_t o, uint32_t mask) {
   return o ^ (((o >> 7) & mask) << 4);
+}
+
+// Final value of one element of C: the accumulated sum, or with the general
+// form alpha * sum + beta * C_old (C_old read only when beta != 0).
+__device__ __forceinline__ float scaled_c(float acc, const float* dst, float alpha, float beta) {
+  const float r = alpha * acc;
+  return beta != 0.0f ? fmaf(beta, *dst, r) : r;
 }
 
 // The operand parts the tensor core is given for one fp32 element: with
@@ -168,10 +185,18 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
   return r != 0;
 }
 
-template <int TM, int BK, int NPROD, bool TMA>
+template <int TM, int BK, int NPROD, int LOAD>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+                   const __grid_constant__ CUtensorMap tmB, const TcParams p,
+                   const TcGeneral gp) {
+  constexpr bool TMA = LOAD == kLoadTma;
+  constexpr bool GEN = LOAD == kLoadStagedGeneral;
+  constexpr bool PLAIN_C = LOAD == kLoadStaged;   // C = the sum, row stride N
+  const int ldc = PLAIN_C ? p.N : gp.ldc;
+  const bool scale = !PLAIN_C && gp.scale;
+  const int lda = GEN ? gp.lda : p.K, ldb = GEN ? gp.ldb : p.N;
+  const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
   using Cfg = TcCfg<TM, BK, NPROD>;
   constexpr int S = Cfg::STAGES;
   constexpr int NACC = Cfg::NACC;
@@ -362,11 +387,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           const int m0 = c.tm * TM + chunk * 32;
           if (n_ok) {
-            float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(p.N) + n;
+            float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(ldc) + n;
             const int rows = min(32, p.M - m0);
+            if (!scale) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < rows) dst[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+              for (int j = 0; j < 32; ++j)
+                if (j < rows) dst[static_cast<size_t>(j) * ldc] = __uint_as_float(v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (j < rows) {
+                  float* d = dst + static_cast<size_t>(j) * ldc;
+                  *d = scaled_c(__uint_as_float(v[j]), d, gp.alpha, gp.beta);
+                }
+              }
+            }
           }
         }
       }
@@ -437,33 +472,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c0 = 0; c0 < AV; c0 += CH) {
             uint32_t av[CH];
-            // A tile: element e = tt + 256 j is row e / BK, column e % BK
-            // (lanes run along k: coalesced)
+            // A tile: element e = tt + 256 j is row r, column k of the tile,
+            // with lanes along k (or along m when A is stored transposed), so
+            // that they read consecutive addresses
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
               const int e = tt + (c0 + j) * kTransformThreads;
-              const int gm = m0 + e / BK, gk = k0 + e % BK;
-              av[j] = (gm < p.M && gk < p.K)
-                          ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
-                          : 0u;
+              const int r = trans_a ? e % TM : e / BK, k = trans_a ? e / TM : e % BK;
+              const int gm = m0 + r, gk = k0 + k;
+              const size_t at = trans_a ? static_cast<size_t>(gk) * lda + gm
+                                          : static_cast<size_t>(gm) * lda + gk;
+              av[j] = (gm < p.M && gk < p.K) ? __float_as_uint(__ldg(p.A + at)) : 0u;
             }
             if (c0 == 0) {
               // B tile: column n0 + col, K rows of this thread's half (lanes along n)
 #pragma unroll
               for (int k = 0; k < KH; ++k) {
                 const int gk = k0 + kh0 + k;
-                bv[k] = (gn < p.N && gk < p.K)
-                            ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
-                            : 0u;
+                const size_t bt_at = trans_b ? static_cast<size_t>(gn) * ldb + gk
+                                               : static_cast<size_t>(gk) * ldb + gn;
+                bv[k] = (gn < p.N && gk < p.K) ? __float_as_uint(__ldg(p.B + bt_at)) : 0u;
               }
             }
 #pragma unroll
             for (int j = 0; j < CH; ++j) {
               const int e = tt + (c0 + j) * kTransformThreads;
+              const int r = trans_a ? e % TM : e / BK, k = trans_a ? e / TM : e % BK;
               uint32_t h, l;
               split_operand<NPROD>(av[j], h, l);
-              const uint32_t o = swizzle(static_cast<uint32_t>((e / BK) * BK * 4 + (e % BK) * 4),
-                                         Cfg::A_SWZ_MASK);
+              const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
               *reinterpret_cast<uint32_t*>(st + o) = h;
               if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
             }
@@ -536,11 +573,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = c.tm * TM + f / (kTN / 4);
           const int n = c.tn * kTN + (f % (kTN / 4)) * 4;
           if (m < p.M) {
-            float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n;
+            float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(ldc) + n;
             const float vals[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (n + q < p.N) dst[q] = vals[q];
+              if (n + q < p.N) dst[q] = scale ? scaled_c(vals[q], dst + q, gp.alpha, gp.beta) : vals[q];
           }
         }
       }
@@ -567,13 +604,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
-// 2-D fp32 map of a row-major [rows x cols] matrix, box [box_rows x box_cols].
-bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_cols, int box_rows,
-               CUtensorMapSwizzle swz) {
+// 2-D fp32 map of a row-major [rows x cols] matrix with row stride ld
+// (elements), box [box_rows x box_cols].
+bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, int box_cols,
+               int box_rows, CUtensorMapSwizzle swz) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4u};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides, box,
@@ -583,12 +621,12 @@ bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_c
 
 constexpr int kMaxDevices = 64;
 
-template <int TM, int BK, int NPROD, bool TMA>
-int launch_one(const GemmArgs& g, const TcParams& p, const CUtensorMap& ma, const CUtensorMap& mb,
-               int grid, cudaStream_t stream) {
+template <int TM, int BK, int NPROD, int LOAD>
+int launch_one(const GemmArgs& g, const TcParams& p, const TcGeneral& gp, const CUtensorMap& ma,
+               const CUtensorMap& mb, int grid, cudaStream_t stream) {
   using Cfg = TcCfg<TM, BK, NPROD>;
   static std::atomic<unsigned long long> configured{0};  // bit per device
-  auto kern = tc_gemm_kernel<TM, BK, NPROD, TMA>;
+  auto kern = tc_gemm_kernel<TM, BK, NPROD, LOAD>;
   const unsigned long long bit = 1ull << (g.device % kMaxDevices);
   if (!(configured.load() & bit)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
@@ -598,31 +636,43 @@ int launch_one(const GemmArgs& g, const TcParams& p, const CUtensorMap& ma, cons
     }
     configured.fetch_or(bit);
   }
-  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p);
+  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p, gp);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;
 }
 
-template <int BK, int NPROD, bool TMA>
-int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const CUtensorMap& ma,
-              const CUtensorMap& mb, int grid, cudaStream_t stream) {
+template <int BK, int NPROD, int LOAD>
+int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const TcGeneral& gp,
+              const CUtensorMap& ma, const CUtensorMap& mb, int grid, cudaStream_t stream) {
   switch (tm) {
-    case 64: return launch_one<64, BK, NPROD, TMA>(g, p, ma, mb, grid, stream);
-    case 128: return launch_one<128, BK, NPROD, TMA>(g, p, ma, mb, grid, stream);
-    default: return launch_one<256, BK, NPROD, TMA>(g, p, ma, mb, grid, stream);
+    case 64: return launch_one<64, BK, NPROD, LOAD>(g, p, gp, ma, mb, grid, stream);
+    case 128: return launch_one<128, BK, NPROD, LOAD>(g, p, gp, ma, mb, grid, stream);
+    default: return launch_one<256, BK, NPROD, LOAD>(g, p, gp, ma, mb, grid, stream);
   }
 }
 
 // Tile heights 64 and 128 are also built with BK = 32 for three products:
 // fewer, larger stages (the MMA thread's wait on a stage costs about as much
 // as the stage's MMAs at these heights).
-template <int NPROD, bool TMA>
-int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const CUtensorMap& ma,
-                 const CUtensorMap& mb, int grid, cudaStream_t stream) {
-  if (NPROD == 1) return launch_tm<32, 1, TMA>(tm, g, p, ma, mb, grid, stream);
-  if (bk == 16) return launch_tm<16, 3, TMA>(tm, g, p, ma, mb, grid, stream);
-  return tm == 64 ? launch_one<64, 32, 3, TMA>(g, p, ma, mb, grid, stream)
-                  : launch_one<128, 32, 3, TMA>(g, p, ma, mb, grid, stream);
+template <int NPROD, int LOAD>
+int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const TcGeneral& gp,
+                 const CUtensorMap& ma, const CUtensorMap& mb, int grid, cudaStream_t stream) {
+  if (NPROD == 1) return launch_tm<32, 1, LOAD>(tm, g, p, gp, ma, mb, grid, stream);
+  if (bk == 16) return launch_tm<16, 3, LOAD>(tm, g, p, gp, ma, mb, grid, stream);
+  return tm == 64 ? launch_one<64, 32, 3, LOAD>(g, p, gp, ma, mb, grid, stream)
+                  : launch_one<128, 32, 3, LOAD>(g, p, gp, ma, mb, grid, stream);
+}
+
+// The loader for a launch: TMA when the operands allow, else the staged
+// loads of the plain product or of the general form.
+template <int NPROD>
+int launch_loader(bool tma, int tm, int bk, const GemmArgs& g, const TcParams& p,
+                  const TcGeneral& gp, const CUtensorMap& ma, const CUtensorMap& mb, int grid,
+                  cudaStream_t stream) {
+  if (tma) return launch_tm_bk<NPROD, kLoadTma>(tm, bk, g, p, gp, ma, mb, grid, stream);
+  if (plain_form(g))
+    return launch_tm_bk<NPROD, kLoadStaged>(tm, bk, g, p, gp, ma, mb, grid, stream);
+  return launch_tm_bk<NPROD, kLoadStagedGeneral>(tm, bk, g, p, gp, ma, mb, grid, stream);
 }
 
 // K depth of a stage: 32 for one product; for three, 32 at tile heights
@@ -630,6 +680,19 @@ int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const CUt
 int bk_for(int nprod, int tm) { return (nprod == 1 || tm <= 128) ? 32 : 16; }
 
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+TcGeneral general_of(const GemmArgs& g) {
+  TcGeneral gp;
+  gp.lda = g.lda;
+  gp.ldb = g.ldb;
+  gp.ldc = g.ldc;
+  gp.trans_a = g.trans_a;
+  gp.trans_b = g.trans_b;
+  gp.alpha = g.alpha;
+  gp.beta = g.beta;
+  gp.scale = g.scale;
+  return gp;
+}
 
 // Tile height TM.  With the split tail the schedule no longer quantises to
 // whole waves, so the most efficient height is used (256; 128 or 64 when M
@@ -675,6 +738,7 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   p.tiles_n = ceil_div(g.N, kTN);
   p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
+  const TcGeneral gp = general_of(g);
   p.partials = nullptr;
   p.counters = nullptr;
   p.sk_ctas = 0;
@@ -728,27 +792,20 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   }
 
   // TMA needs 16-byte aligned bases and row strides (K % 4 == 0, N % 4 == 0).
-  bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && g.K % 4 == 0 && g.N % 4 == 0 &&
-             reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
-             reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+  bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && tma_addressable(g);
   alignas(64) CUtensorMap ma, mb;
   if (tma) {
-    tma = encode_2d(&ma, g.A, g.M, g.K, bk, tm,
+    tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, tm,
                     bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+          encode_2d(&mb, g.B, g.K, g.N, g.ldb, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!tma) {
     memset(&ma, 0, sizeof(ma));
     memset(&mb, 0, sizeof(mb));
   }
-  int rc;
-  if (nprod == 3) {
-    rc = tma ? launch_tm_bk<3, true>(tm, bk, g, p, ma, mb, grid, stream)
-             : launch_tm_bk<3, false>(tm, bk, g, p, ma, mb, grid, stream);
-  } else {
-    rc = tma ? launch_tm_bk<1, true>(tm, bk, g, p, ma, mb, grid, stream)
-             : launch_tm_bk<1, false>(tm, bk, g, p, ma, mb, grid, stream);
-  }
+  const int rc = nprod == 3
+                     ? launch_loader<3>(tma, tm, bk, g, p, gp, ma, mb, grid, stream)
+                     : launch_loader<1>(tma, tm, bk, g, p, gp, ma, mb, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "tc_gemm_kernel";
@@ -798,6 +855,7 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
   p.tiles_n = ceil_div(g.N, kTN);
   p.drop_first_copy = 0;
   p.err = g.err;
+  const TcGeneral gp = general_of(g);
   p.partials = nullptr;
   p.counters = nullptr;
   int tm = choose_tm(g, true);
@@ -835,26 +893,20 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
     grid = static_cast<int>(std::min<long>(tiles, g.num_sms));
   }
 
-  bool tma = g.K % 4 == 0 && g.N % 4 == 0 && reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
-             reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
+  bool tma = tma_addressable(g);
   alignas(64) CUtensorMap ma, mb;
   if (tma) {
-    tma = encode_2d(&ma, g.A, g.M, g.K, bk, tm,
+    tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, tm,
                     bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+          encode_2d(&mb, g.B, g.K, g.N, g.ldb, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!tma) {
     memset(&ma, 0, sizeof(ma));
     memset(&mb, 0, sizeof(mb));
   }
-  int rc;
-  if (nprod == 3) {
-    rc = tma ? launch_tm_bk<3, true>(tm, bk, g, p, ma, mb, grid, stream)
-             : launch_tm_bk<3, false>(tm, bk, g, p, ma, mb, grid, stream);
-  } else {
-    rc = tma ? launch_tm_bk<1, true>(tm, bk, g, p, ma, mb, grid, stream)
-             : launch_tm_bk<1, false>(tm, bk, g, p, ma, mb, grid, stream);
-  }
+  const int rc = nprod == 3
+                     ? launch_loader<3>(tma, tm, bk, g, p, gp, ma, mb, grid, stream)
+                     : launch_loader<1>(tma, tm, bk, g, p, gp, ma, mb, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "tc_gemm_kernel";

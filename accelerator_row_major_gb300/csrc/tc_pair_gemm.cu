@@ -72,6 +72,21 @@ struct PairParams {
   unsigned* err;
 };
 
+// The general form (see tc_gemm.cu): a separate kernel argument.
+struct PairGeneral {
+  int lda, ldb, ldc;
+  int trans_a, trans_b;
+  float alpha, beta;
+  int scale;
+};
+
+// alpha * acc (+ beta * C_old, read only when beta != 0).
+__device__ __forceinline__ float pair_scaled_c(float acc, const float* dst, float alpha,
+                                              float beta) {
+  const float r = alpha * acc;
+  return beta != 0.0f ? fmaf(beta, *dst, r) : r;
+}
+
 template <int BK, int NPROD>
 struct PairCfg {
   static constexpr int A_BYTES = kHalf * BK * 4;
@@ -280,10 +295,17 @@ struct PairWorkList {
   }
 };
 
-template <int BK, int NPROD, bool TMA>
+template <int BK, int NPROD, int LOAD>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const PairParams p) {
+                   const PairParams p, const PairGeneral gp) {
+  constexpr bool TMA = LOAD == kLoadTma;
+  constexpr bool GEN = LOAD == kLoadStagedGeneral;
+  constexpr bool PLAIN_C = LOAD == kLoadStaged;   // C = the sum, row stride N
+  const int ldc = PLAIN_C ? p.N : gp.ldc;
+  const bool scale = !PLAIN_C && gp.scale;
+  const int lda = GEN ? gp.lda : p.K, ldb = GEN ? gp.ldb : p.N;
+  const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
   using Cfg = PairCfg<BK, NPROD>;
   constexpr int S = Cfg::STAGES;
   extern __shared__ uint8_t smem_dyn[];
@@ -492,11 +514,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_ld();
           const int m0 = c.tm * kPairTile + chunk * 32;
           if (n_ok) {
-            float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(p.N) + n;
+            float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(ldc) + n;
             const int rows = min(32, p.M - m0);
+            if (!scale) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < rows) dst[static_cast<size_t>(j) * p.N] = __uint_as_float(v[j]);
+              for (int j = 0; j < 32; ++j)
+                if (j < rows) dst[static_cast<size_t>(j) * ldc] = __uint_as_float(v[j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                if (j < rows) {
+                  float* d = dst + static_cast<size_t>(j) * ldc;
+                  *d = pair_scaled_c(__uint_as_float(v[j]), d, gp.alpha, gp.beta);
+                }
+              }
+            }
           }
         }
       }
@@ -552,36 +584,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int m0 = c.tm * kPairTile + static_cast<int>(rank) * kHalf;
           const int n0 = c.tn * kPairTile + static_cast<int>(rank) * kHalf;
           const int k0 = kt * BK;
-          // All of this thread's loads for the stage are issued before any
-          // of them is used, so one latency covers the stage.
-          constexpr int AV = kHalf * BK / (kTransformWarps * 32);   // 8 or 16
-          uint32_t av[AV], bv[KH];
-#pragma unroll
-          for (int j = 0; j < AV; ++j) {
-            // element e = tt + 256 j: row e / BK, column e % BK (lanes along k)
-            const int e = tt + j * kTransformWarps * 32;
-            const int gm = m0 + e / BK, gk = k0 + e % BK;
-            av[j] = (gm < p.M && gk < p.K)
-                        ? __float_as_uint(__ldg(p.A + static_cast<size_t>(gm) * p.K + gk))
-                        : 0u;
-          }
+          // This thread's loads for the stage are all issued before any of
+          // them is used, so one latency covers the stage.
+          constexpr int AV = kHalf * BK / (kTransformWarps * 32);   // 8
+          constexpr int CH = AV;
+          uint32_t bv[KH];
           const int gn = n0 + col;
 #pragma unroll
-          for (int k = 0; k < KH; ++k) {
-            const int gk = k0 + kh0 + k;
-            bv[k] = (gn < p.N && gk < p.K)
-                        ? __float_as_uint(__ldg(p.B + static_cast<size_t>(gk) * p.N + gn))
-                        : 0u;
-          }
+          for (int c0 = 0; c0 < AV; c0 += CH) {
+            uint32_t av[CH];
 #pragma unroll
-          for (int j = 0; j < AV; ++j) {
-            const int e = tt + j * kTransformWarps * 32;
-            uint32_t h, l;
-            split_operand<NPROD>(av[j], h, l);
-            const uint32_t o = swizzle(static_cast<uint32_t>((e / BK) * BK * 4 + (e % BK) * 4),
-                                       Cfg::A_SWZ_MASK);
-            *reinterpret_cast<uint32_t*>(st + o) = h;
-            if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+            for (int j = 0; j < CH; ++j) {
+              // element e = tt + 256 j: row r, column k of the half tile, lanes
+              // along k (along m when A is stored transposed)
+              const int e = tt + (c0 + j) * kTransformWarps * 32;
+              const int r = trans_a ? e % kHalf : e / BK, k = trans_a ? e / kHalf : e % BK;
+              const int gm = m0 + r, gk = k0 + k;
+              const size_t at = trans_a ? static_cast<size_t>(gk) * lda + gm
+                                          : static_cast<size_t>(gm) * lda + gk;
+              av[j] = (gm < p.M && gk < p.K) ? __float_as_uint(__ldg(p.A + at)) : 0u;
+            }
+            if (c0 == 0) {
+#pragma unroll
+              for (int k = 0; k < KH; ++k) {
+                const int gk = k0 + kh0 + k;
+                const size_t bt_at = trans_b ? static_cast<size_t>(gn) * ldb + gk
+                                               : static_cast<size_t>(gk) * ldb + gn;
+                bv[k] = (gn < p.N && gk < p.K) ? __float_as_uint(__ldg(p.B + bt_at)) : 0u;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+              const int e = tt + (c0 + j) * kTransformWarps * 32;
+              const int r = trans_a ? e % kHalf : e / BK, k = trans_a ? e / kHalf : e % BK;
+              uint32_t h, l;
+              split_operand<NPROD>(av[j], h, l);
+              const uint32_t o = swizzle(static_cast<uint32_t>(r * BK * 4 + k * 4), Cfg::A_SWZ_MASK);
+              *reinterpret_cast<uint32_t*>(st + o) = h;
+              if (NPROD == 3) *reinterpret_cast<uint32_t*>(st + Cfg::A_BYTES + o) = l;
+            }
           }
 #pragma unroll
           for (int k = 0; k < KH; ++k) split_operand<NPROD>(bv[k], bh[k], bl[k]);
@@ -651,11 +692,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int m = c.tm * kPairTile + f / (kHalf / 4);
           const int n = c.tn * kPairTile + static_cast<int>(rank) * kHalf + (f % (kHalf / 4)) * 4;
           if (m < p.M) {
-            float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(p.N) + n;
+            float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(ldc) + n;
             const float vals[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq)
-              if (n + qq < p.N) dst[qq] = vals[qq];
+              if (n + qq < p.N)
+                dst[qq] = scale ? pair_scaled_c(vals[qq], dst + qq, gp.alpha, gp.beta) : vals[qq];
           }
         }
       }
@@ -668,8 +710,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
-bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_cols, int box_rows,
-               CUtensorMapSwizzle swz) {
+bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, int box_cols,
+               int box_rows, CUtensorMapSwizzle swz) {
   std::call_once(g_encode_once, [] {
     void* fn = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -682,7 +724,7 @@ bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_c
   });
   if (!g_encode) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4u};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
@@ -692,12 +734,12 @@ bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int box_c
 
 constexpr int kMaxDevices = 64;
 
-template <int BK, int NPROD, bool TMA>
-int launch_pair_one(const GemmArgs& g, const PairParams& p, const CUtensorMap& ma,
-                    const CUtensorMap& mb, int grid, cudaStream_t stream) {
+template <int BK, int NPROD, int LOAD>
+int launch_pair_one(const GemmArgs& g, const PairParams& p, const PairGeneral& gp,
+                    const CUtensorMap& ma, const CUtensorMap& mb, int grid, cudaStream_t stream) {
   using Cfg = PairCfg<BK, NPROD>;
   static std::atomic<unsigned long long> configured{0};
-  auto kern = tc_pair_kernel<BK, NPROD, TMA>;
+  auto kern = tc_pair_kernel<BK, NPROD, LOAD>;
   const unsigned long long bit = 1ull << (g.device % kMaxDevices);
   if (!(configured.load() & bit)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
@@ -707,7 +749,7 @@ int launch_pair_one(const GemmArgs& g, const PairParams& p, const CUtensorMap& m
     }
     configured.fetch_or(bit);
   }
-  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p);
+  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p, gp);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;
 }
@@ -727,9 +769,24 @@ bool tc_pair_suits(const GemmArgs& g) {
 
 int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   *launches = 0;
-  const int bk = nprod == 3 ? 16 : 32;
   const int pairs = g.num_sms / 2;
   if (pairs < 1) return GEMM_F32_EDEVICE;
+  // Operand path first: it sets the K depth of a stage (one product on the
+  // TMA path: 32; otherwise 16, which keeps the staged loads of one product
+  // within the 96 registers this 18-warp block gets).
+  bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && tma_addressable(g);
+  int bk = (nprod == 1 && tma) ? 32 : 16;
+  alignas(64) CUtensorMap ma, mb;
+  if (tma) {
+    tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, kHalf,
+                    bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
+          encode_2d(&mb, g.B, g.K, g.N, g.ldb, kHalf, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+  }
+  if (!tma) {
+    bk = 16;
+    memset(&ma, 0, sizeof(ma));
+    memset(&mb, 0, sizeof(mb));
+  }
   PairParams p;
   p.A = g.A;
   p.B = g.B;
@@ -742,6 +799,15 @@ int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   p.k_iters = (g.K + bk - 1) / bk;
   p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
+  PairGeneral gp;
+  gp.lda = g.lda;
+  gp.ldb = g.ldb;
+  gp.ldc = g.ldc;
+  gp.trans_a = g.trans_a;
+  gp.trans_b = g.trans_b;
+  gp.alpha = g.alpha;
+  gp.beta = g.beta;
+  gp.scale = g.scale;
   p.partials = nullptr;
   p.counters = nullptr;
   const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
@@ -772,27 +838,15 @@ int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
     }
   }
   const int grid = 2 * units;
-
-  bool tma = !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && g.K % 4 == 0 && g.N % 4 == 0 &&
-             reinterpret_cast<uintptr_t>(g.A) % 16 == 0 &&
-             reinterpret_cast<uintptr_t>(g.B) % 16 == 0;
-  alignas(64) CUtensorMap ma, mb;
-  if (tma) {
-    tma = encode_2d(&ma, g.A, g.M, g.K, bk, kHalf,
-                    bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, kHalf, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  if (!tma) {
-    memset(&ma, 0, sizeof(ma));
-    memset(&mb, 0, sizeof(mb));
-  }
   int rc;
   if (nprod == 3)
-    rc = tma ? launch_pair_one<16, 3, true>(g, p, ma, mb, grid, stream)
-             : launch_pair_one<16, 3, false>(g, p, ma, mb, grid, stream);
+    rc = tma ? launch_pair_one<16, 3, kLoadTma>(g, p, gp, ma, mb, grid, stream)
+         : plain_form(g) ? launch_pair_one<16, 3, kLoadStaged>(g, p, gp, ma, mb, grid, stream)
+                         : launch_pair_one<16, 3, kLoadStagedGeneral>(g, p, gp, ma, mb, grid, stream);
   else
-    rc = tma ? launch_pair_one<32, 1, true>(g, p, ma, mb, grid, stream)
-             : launch_pair_one<32, 1, false>(g, p, ma, mb, grid, stream);
+    rc = tma ? launch_pair_one<32, 1, kLoadTma>(g, p, gp, ma, mb, grid, stream)
+         : plain_form(g) ? launch_pair_one<16, 1, kLoadStaged>(g, p, gp, ma, mb, grid, stream)
+                         : launch_pair_one<16, 1, kLoadStagedGeneral>(g, p, gp, ma, mb, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "tc_pair_kernel";

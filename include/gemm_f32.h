@@ -127,7 +127,8 @@ int gemm_f32_last_launches(void);
 /* Name of the kernel the last successful call on this host thread launched:
  * "tc_pair_kernel" (tensor cores, 256 x 256 tiles on SM pairs),
  * "tc_gemm_kernel" (tensor cores, one SM per tile), "ffma_gemm_kernel",
- * "memset" (K == 0), "ladder_v0" .. "ladder_v4" (gemm_f32_ladder) or
+ * "memset" (K == 0), "scale_window_kernel" (gemm_f32_general with
+ * alpha == 0 or K == 0), "ladder_v0" .. "ladder_v4" (gemm_f32_ladder) or
  * "none" (nothing launched).  Static string. */
 const char* gemm_f32_last_kernel(void);
 
@@ -162,6 +163,36 @@ int gemm_f32_release(void);
  * The result equals gemm_f32_ex's for the same mode. */
 int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                      int mode, gemm_f32_stream_t stream);
+
+/* General form, row-major storage throughout:
+ *     C = alpha * op(A) * op(B) + beta * C
+ * the scaled, strided and transposable product of the cuBLAS call on
+ * "LeetGPU problem 2: matrix multiplication" (yekq.top, section "cuBLAS
+ * reference"), restated for row-major matrices.
+ *   op(A) is M x K: trans_a = 0, A is stored M x K with row stride lda
+ *     (lda >= max(1, K)); trans_a = 1, A is stored K x M (lda >= max(1, M))
+ *     and op(A) is its transpose.
+ *   op(B) is K x N: trans_b = 0, B is stored K x N (ldb >= max(1, N));
+ *     trans_b = 1, B is stored N x K (ldb >= max(1, K)).
+ *   C is the M x N window of a row-major array with row stride ldc
+ *     (ldc >= max(1, N)); nothing outside the window is read or written.
+ *   beta == 0: C is not read (whatever it holds, NaN included, is
+ *     overwritten).  alpha == 0 or K == 0: A and B are not read and
+ *     C = beta * C.
+ *   mode: GEMM_F32_MODE_TC3X, _FFMA or _TC1X with the bounds of gemm_f32_ex,
+ *     taken relative to |alpha| (|op(A)||op(B)|)_ij + |beta| |C_ij|.
+ * Untransposed operands with row strides a multiple of 4 and 16-byte
+ * aligned bases take the tensor-memory-accelerator path; any other layout
+ * the per-thread staged loads (slower, same results).
+ * Device pointers, caller-owned; asynchronous on `stream`.  Returns 0,
+ * GEMM_F32_EINVAL (trans flag not 0/1, a negative size, a stride below its
+ * minimum, alpha or beta not finite, a null or misaligned pointer that
+ * would be used, or the C window overlapping a stored A or B window),
+ * GEMM_F32_EDEVICE or GEMM_F32_ELAUNCH.  May allocate the split-tail
+ * workspace as gemm_f32_ex does. */
+int gemm_f32_general(int trans_a, int trans_b, int M, int N, int K, float alpha,
+                     const float* A, int lda, const float* B, int ldb, float beta, float* C,
+                     int ldc, int mode, gemm_f32_stream_t stream);
 
 /* The pages' optimisation ladder for this GEMM ("LeetGPU problem 2: matrix
  * multiplication", yekq.top, sections v0 .. v4 and "benchmark summary"),

@@ -112,3 +112,34 @@ def sample_indices(M, N, count, seed):
 
 def oracle_full(A, B):
     return oracle.gemm(A, B)
+
+
+def run_general(A_store, B_store, C_store, M, N, K, alpha, beta, trans_a=0, trans_b=0, mode="tc3x"):
+    """gemm_f32_general on cuda:0 with the stored arrays as given (row strides
+    = their widths).  C_store sits inside a sentinel guard band; checks that
+    nothing outside the M x N window of C changed and returns the new C_store."""
+    import torch
+
+    g = lib()
+    dev = torch.device("cuda:0")
+    a = torch.from_numpy(np.ascontiguousarray(A_store)).to(dev)
+    b = torch.from_numpy(np.ascontiguousarray(B_store)).to(dev)
+    C_store = np.ascontiguousarray(C_store, dtype=np.float32)
+    flat = np.concatenate([np.full(GUARD, SENTINEL, np.uint32), C_store.reshape(-1).view(np.uint32),
+                           np.full(GUARD, SENTINEL, np.uint32)])
+    c = torch.from_numpy(flat.view(np.float32).copy()).to(dev)
+    s = torch.cuda.current_stream(dev)
+    rc = g.gemm_f32_general(trans_a, trans_b, M, N, K, alpha, a.data_ptr(), A_store.shape[1],
+                            b.data_ptr(), B_store.shape[1], beta, c.data_ptr() + 4 * GUARD,
+                            C_store.shape[1], mode, s)
+    assert rc == g.GEMM_F32_OK, "gemm_f32_general returned %d" % rc
+    st, site = g.gemm_f32_status(s)
+    assert st == g.GEMM_F32_OK, "device error word: site %d" % site
+    host = c.cpu().numpy().view(np.uint32)
+    assert np.all(host[:GUARD] == SENTINEL) and np.all(host[-GUARD:] == SENTINEL), "write outside C"
+    out = host[GUARD:-GUARD].view(np.float32).reshape(C_store.shape).copy()
+    outside = np.ones(C_store.shape, bool)
+    outside[:M, :N] = False
+    assert np.array_equal(out.view(np.uint32)[outside], C_store.view(np.uint32)[outside]), \
+        "a write landed in C's padding"
+    return out

@@ -22,6 +22,7 @@ def g():
 def test_header_declares_the_entry_points(g):
     names = g.declared_symbols()
     assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status", "gemm_f32_ladder",
+                            "gemm_f32_general",
                             "gemm_f32_last_kernel", "gemm_f32_last_launches", "gemm_f32_noalloc",
                             "gemm_f32_release",
                             "gemm_f32_version"])
@@ -76,6 +77,46 @@ def test_ladder_rejects_malformed_requests_on_the_host(g, args, step):
     assert g.gemm_f32_last_launches() == 0
 
 
+# (trans_a, trans_b, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, mode)
+GOOD = (0, 0, 4, 4, 4, 1.0, FAKE_A, 4, FAKE_B, 4, 0.0, FAKE_C, 4, 0)
+
+
+def _with(**kw):
+    names = ["ta", "tb", "M", "N", "K", "alpha", "A", "lda", "B", "ldb", "beta", "C", "ldc", "mode"]
+    args = dict(zip(names, GOOD))
+    args.update(kw)
+    return tuple(args[n] for n in names)
+
+
+@pytest.mark.parametrize("args", [
+    _with(ta=2),                              # trans flag not 0/1
+    _with(tb=-1),
+    _with(M=-1),
+    _with(lda=3),                             # lda < K
+    _with(ta=1, M=6, lda=5),                  # stored K x M needs lda >= M
+    _with(ldb=3),                             # ldb < N
+    _with(tb=1, K=6, ldb=5),                  # stored N x K needs ldb >= K
+    _with(ldc=3),                             # ldc < N
+    _with(alpha=float("nan")),
+    _with(beta=float("inf")),
+    _with(mode=9),
+    _with(C=0),
+    _with(A=0),
+    _with(B=FAKE_B + 2),                      # misaligned
+    _with(C=FAKE_A + 4 * 4 * 3),              # C window starts inside A's last row
+    _with(ldc=64, C=FAKE_B - 64 * 4 * 3),     # strided C window reaches into B
+])
+def test_general_rejects_malformed_requests_on_the_host(g, args):
+    assert g.gemm_f32_general(*args) == g.GEMM_F32_EINVAL
+    assert g.gemm_f32_last_launches() == 0
+
+
+def test_general_alpha_zero_needs_no_operands(g):
+    # alpha == 0: A and B are not used, so they may be null; no GPU here
+    rc = g.gemm_f32_general(*_with(alpha=0.0, A=0, B=0))
+    assert rc == g.GEMM_F32_EDEVICE
+
+
 def test_empty_outputs_are_a_no_op(g):
     # M == 0 or N == 0: nothing to write, no CUDA call, success
     assert g.gemm_f32_ex(FAKE_A, FAKE_B, FAKE_C, 0, 5, 5) == g.GEMM_F32_OK
@@ -85,6 +126,7 @@ def test_empty_outputs_are_a_no_op(g):
     assert g.gemm_f32_last_launches() == 0
     for step in range(5):
         assert g.gemm_f32_ladder(FAKE_A, FAKE_B, FAKE_C, 0, 5, 5, step) == g.GEMM_F32_OK
+    assert g.gemm_f32_general(*_with(M=0)) == g.GEMM_F32_OK
     assert g.gemm_f32_last_kernel() == "none"
 
 
