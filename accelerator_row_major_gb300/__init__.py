@@ -13,7 +13,7 @@ from ._binding import (FLAG_CTA_PAIR, FLAG_FORCE_STAGED, FLAG_SINGLE_CTA, FLAG_T
                        FLAG_NO_SPLIT_K, FLAG_ONE_TILE_PER_CTA, FLAG_TEST_DROP_COPY, GEMM_F32_EDEVICE, GEMM_F32_EINVAL,
                        GEMM_F32_ELAUNCH, GEMM_F32_ESCRATCH, GEMM_F32_ETIMEOUT, GEMM_F32_OK, LIB_PATH, MODE_FFMA,
                        MODE_TC1X, MODE_TC3X, MODES, GemmError, check, declared_symbols,
-                       gemm_f32, gemm_f32_ex, gemm_f32_general, gemm_f32_ladder, gemm_f32_last_kernel, gemm_f32_last_launches,
+                       gemm_f32, gemm_f32_ex, gemm_f32_general, gemm_f32_host, gemm_f32_ladder, gemm_f32_last_kernel, gemm_f32_last_launches,
                        gemm_f32_noalloc, LADDER_STEPS,
                        gemm_f32_release, NOALLOC_SCRATCH_BYTES,
                        gemm_f32_status,

@@ -70,6 +70,8 @@ def _load() -> ctypes.CDLL:
     cf = ctypes.c_float
     lib.gemm_f32_general.argtypes = [ci, ci, ci, ci, ci, cf, vp, ci, vp, ci, cf, vp, ci, ci, vp]
     lib.gemm_f32_general.restype = ci
+    lib.gemm_f32_host.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
+    lib.gemm_f32_host.restype = ci
     lib.gemm_f32_ladder.argtypes = [vp, vp, vp, ci, ci, ci, ci, vp]
     lib.gemm_f32_ladder.restype = ci
     lib.gemm_f32_last_kernel.argtypes = []
@@ -105,7 +107,9 @@ def _ptr(x) -> int:
         return 0
     if isinstance(x, int):
         return x
-    return int(x.data_ptr())
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    return int(x.ctypes.data)          # numpy array (host memory)
 
 
 def _stream(s) -> int:
@@ -145,6 +149,15 @@ def gemm_f32_general(trans_a: int, trans_b: int, M: int, N: int, K: int, alpha: 
         mode = MODES[mode]
     return lib().gemm_f32_general(int(trans_a), int(trans_b), M, N, K, float(alpha), _ptr(A), lda,
                                   _ptr(B), ldb, float(beta), _ptr(C), ldc, int(mode), _stream(stream))
+
+
+def gemm_f32_host(A, B, C, M: int, N: int, K: int, mode=MODE_TC3X, stream=None) -> int:
+    """C = A * B with A, B, C in host memory (pinned torch tensors, numpy
+    arrays or addresses); copies and product are queued on the library's
+    streams, and `stream` waits for C (see include/gemm_f32.h)."""
+    if isinstance(mode, str):
+        mode = MODES[mode]
+    return lib().gemm_f32_host(_ptr(A), _ptr(B), _ptr(C), M, N, K, int(mode), _stream(stream))
 
 
 LADDER_STEPS = (0, 1, 2, 3, 4)

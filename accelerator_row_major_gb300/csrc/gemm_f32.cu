@@ -351,6 +351,131 @@ extern "C" int gemm_f32_general(int trans_a, int trans_b, int M, int N, int K, f
   return rc;
 }
 
+// ---------------------------------------------------------------- host buffers
+// gemm_f32_host: per device, three streams (copy in, product, copy out) and
+// two device slots taken by alternate calls, so that the copies of one call
+// overlap the product of its neighbour.  Events order every reuse of a slot:
+// its A and B are overwritten only after the product that read them, its C
+// only after the copy that drained it.
+namespace {
+
+struct HostSlot {
+  float* A = nullptr;
+  float* B = nullptr;
+  float* C = nullptr;
+  size_t a_cap = 0, b_cap = 0, c_cap = 0;   // bytes
+  cudaEvent_t loaded = nullptr, computed = nullptr, drained = nullptr;
+  bool used = false;
+};
+
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+  HostSlot slot[2];
+  int next = 0;
+};
+
+HostPipe g_pipes[kMaxDevices];
+
+bool host_pipe_init(HostPipe& hp) {
+  if (hp.ready) return true;
+  for (cudaStream_t* s : {&hp.in, &hp.comp, &hp.out})
+    if (cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) != cudaSuccess) return false;
+  for (HostSlot& sl : hp.slot)
+    for (cudaEvent_t* e : {&sl.loaded, &sl.computed, &sl.drained})
+      if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return false;
+  hp.ready = true;
+  return true;
+}
+
+// Device buffer of at least `need` bytes (1 MiB granules), reallocated only
+// when it must grow; the caller has made sure no queued work still uses it.
+bool host_slot_buffer(float** p, size_t* cap, size_t need) {
+  if (*cap >= need) return true;
+  if (*p) (void)cudaFree(*p);
+  *p = nullptr;
+  *cap = 0;
+  const size_t want = (need + (1u << 20) - 1) & ~static_cast<size_t>((1u << 20) - 1);
+  if (cudaMalloc(reinterpret_cast<void**>(p), want) != cudaSuccess) return false;
+  *cap = want;
+  return true;
+}
+
+void host_pipe_free(HostPipe& hp) {
+  for (HostSlot& sl : hp.slot) {
+    for (float** b : {&sl.A, &sl.B, &sl.C}) {
+      if (*b) (void)cudaFree(*b);
+      *b = nullptr;
+    }
+    sl.a_cap = sl.b_cap = sl.c_cap = 0;
+    sl.used = false;
+  }
+}
+
+}  // namespace
+
+extern "C" int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K,
+                             int mode, gemm_f32_stream_t stream_handle) {
+  t_last_launches = 0;
+  t_last_kernel = "none";
+  if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_FFMA && mode != GEMM_F32_MODE_TC1X)
+    return GEMM_F32_EINVAL;
+  const int chk = check_operands(A, B, C, M, N, K);
+  if (chk != 0) return chk < 0 ? chk : GEMM_F32_OK;
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
+  const size_t a_bytes = static_cast<size_t>(M) * K * sizeof(float);
+  const size_t b_bytes = static_cast<size_t>(K) * N * sizeof(float);
+  const size_t c_bytes = static_cast<size_t>(M) * N * sizeof(float);
+
+  HostPipe& hp = g_pipes[dev];
+  std::lock_guard<std::mutex> lock(hp.mu);
+  auto fail = [] {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  };
+  if (!host_pipe_init(hp)) return fail();
+  HostSlot& sl = hp.slot[hp.next];
+  hp.next ^= 1;
+  if (sl.a_cap < a_bytes || sl.b_cap < b_bytes || sl.c_cap < c_bytes) {
+    if (sl.used && cudaEventSynchronize(sl.drained) != cudaSuccess) return fail();
+    if (!host_slot_buffer(&sl.A, &sl.a_cap, a_bytes) ||
+        !host_slot_buffer(&sl.B, &sl.b_cap, b_bytes) ||
+        !host_slot_buffer(&sl.C, &sl.c_cap, c_bytes)) {
+      host_pipe_free(hp);
+      return fail();
+    }
+  }
+  // copy in, once the product that last read this slot is done
+  if (sl.used && cudaStreamWaitEvent(hp.in, sl.computed, 0) != cudaSuccess) return fail();
+  if (a_bytes && cudaMemcpyAsync(sl.A, A, a_bytes, cudaMemcpyHostToDevice, hp.in) != cudaSuccess)
+    return fail();
+  if (b_bytes && cudaMemcpyAsync(sl.B, B, b_bytes, cudaMemcpyHostToDevice, hp.in) != cudaSuccess)
+    return fail();
+  if (cudaEventRecord(sl.loaded, hp.in) != cudaSuccess) return fail();
+  // the product, once the operands are in and this slot's last C has drained
+  if (cudaStreamWaitEvent(hp.comp, sl.loaded, 0) != cudaSuccess) return fail();
+  if (sl.used && cudaStreamWaitEvent(hp.comp, sl.drained, 0) != cudaSuccess) return fail();
+  const int rc = gemm_f32_ex(sl.A, sl.B, sl.C, M, N, K, mode, 0u,
+                             reinterpret_cast<gemm_f32_stream_t>(hp.comp));
+  if (rc != GEMM_F32_OK) return rc;
+  const int launches = t_last_launches;
+  const char* kernel = t_last_kernel;
+  if (cudaEventRecord(sl.computed, hp.comp) != cudaSuccess) return fail();
+  // copy out, then the caller's stream waits for it
+  if (cudaStreamWaitEvent(hp.out, sl.computed, 0) != cudaSuccess) return fail();
+  if (cudaMemcpyAsync(C, sl.C, c_bytes, cudaMemcpyDeviceToHost, hp.out) != cudaSuccess) return fail();
+  if (cudaEventRecord(sl.drained, hp.out) != cudaSuccess) return fail();
+  sl.used = true;
+  if (cudaStreamWaitEvent(stream, sl.drained, 0) != cudaSuccess) return fail();
+  t_last_launches = launches;
+  t_last_kernel = kernel;
+  return GEMM_F32_OK;
+}
+
 extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                                 int mode, gemm_f32_stream_t stream_handle) {
   t_last_launches = 0;
@@ -433,6 +558,8 @@ extern "C" int gemm_f32_release(void) {
   int dev = 0;
   DeviceState* st = device_state(&dev);
   if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  // same lock order as gemm_f32_host: its pipe, then the workspaces
+  std::lock_guard<std::mutex> hlock(g_pipes[dev].mu);
   std::lock_guard<std::mutex> lock(st->ws_mu);
   int rc = GEMM_F32_OK;
   if (cudaDeviceSynchronize() != cudaSuccess) {
@@ -442,6 +569,7 @@ extern "C" int gemm_f32_release(void) {
   for (auto& kv : st->ws)
     if (kv.second.ptr) (void)cudaFree(kv.second.ptr);
   st->ws.clear();
+  host_pipe_free(g_pipes[dev]);
   return rc;
 }
 

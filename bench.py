@@ -11,8 +11,10 @@ events on the launching stream, bracketed by a barrier and a synchronise.
 Problems whose operands fit twice in L2 get an L2 flush between steps
 (each step timed on its own); the default 8192^3 problem's operands are
 larger than L2.  `value` is whole-job TFLOPS = 2MNK * ranks / max-over-ranks
-time.  The e2e figure times the same call with host buffers: pinned host ->
-device copies of A and B, the product, and the device -> host copy of C.
+time.  The e2e figure times gemm_f32_host, the C-ABI call on host buffers:
+every step copies A and B in from pinned host memory, computes and copies C
+back; consecutive calls overlap one's copies with the next one's product.
+The latency of one such call, waited for alone, is reported beside it.
 
 With N > 1 (torchrun) every rank runs its own replica of the problem on its
 own GPU: the product needs no exchange between GPUs, so scaling is weak.
@@ -168,25 +170,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def source_hash() -> str:
+# the sources each kernel is compiled from (its own file and the shared headers)
+KERNEL_SOURCES = {
+    "tc_pair_kernel": ("tc_pair_gemm.cu", "device_common.cuh", "launch.h"),
+    "tc_gemm_kernel": ("tc_gemm.cu", "device_common.cuh", "launch.h"),
+    "ffma_gemm_kernel": ("ffma_gemm.cu", "device_common.cuh", "launch.h"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """Hash of the sources `kernel` is built from: a recorded ncu figure is
+    used only while they are unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "accelerator_row_major_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(kernel: str, config: str, mode: str):
     """DRAM bytes per launch from a committed ncu capture of the same sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
-    if not os.path.exists(path):
+    if not os.path.exists(path) or kernel not in KERNEL_SOURCES:
         return None
     with open(path) as f:
         table = json.load(f)
     rec = table.get("%s/%s/%s" % (kernel, config, mode))
-    if not rec or rec.get("source_sha") != source_hash():
+    if not rec or rec.get("source_sha") != source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -320,7 +331,7 @@ def run_ours(args):
     ms_per_step = max_over_ranks(device_ms / args.steps, dist_mod, device)
     value = whole_job_tflops(flop, args.steps, world, ms_per_step * args.steps / 1e3)
 
-    # ---- end to end through the public call with host buffers
+    # ---- end to end through the C-ABI call with host buffers
     e2e = None
     if not args.no_e2e:
         A_pin = torch.from_numpy(A_h).pin_memory()
@@ -328,29 +339,45 @@ def run_ours(args):
         C_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
         e2e_steps = max(3, args.steps // 4)
 
-        def e2e_step():
-            A.copy_(A_pin, non_blocking=True)
-            B.copy_(B_pin, non_blocking=True)
-            step()
-            C_pin.copy_(C, non_blocking=True)
+        def e2e_call():
+            # copies A and B in, computes, copies C out (gemm_f32_host)
+            rc = g.gemm_f32_host(A_pin, B_pin, C_pin, M, N, K, args.mode, stream)
+            if rc != 0:
+                raise g.GemmError(rc, "gemm_f32_host")
 
-        with torch.cuda.stream(stream):
-            e2e_step()
+        for _ in range(2):          # both device slots allocated before timing
+            e2e_call()
         torch.cuda.synchronize(device)
         barrier(dist_mod, device)
-        with torch.cuda.stream(stream):
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(e2e_steps):
-                e2e_step()
-            e1.record(stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_call()
+        e1.record(stream)
         torch.cuda.synchronize(device)
         barrier(dist_mod, device)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, dist_mod, device)
+        # the same call waited for one at a time: one product's latency
+        serial = []
+        for _ in range(3):
+            s0 = torch.cuda.Event(enable_timing=True)
+            s1 = torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            e2e_call()
+            s1.record(stream)
+            s1.synchronize()
+            serial.append(s0.elapsed_time(s1))
+        serial_ms = max_over_ranks(statistics.median(serial), dist_mod, device)
         e2e = {"value": whole_job_tflops(flop, 1, world, e2e_ms / 1e3), "unit": "TFLOPS",
                "h2d_bytes_per_step": 4 * (M * K + K * N), "d2h_bytes_per_step": 4 * M * N,
-               "steps": e2e_steps, "ms_per_step": e2e_ms}
+               "steps": e2e_steps, "ms_per_step": e2e_ms,
+               "call": "gemm_f32_host (C ABI) on pinned host buffers, mode %s" % args.mode,
+               "schedule": "calls queued back to back; each copies its A and B in and its C out, "
+                           "and one call's copies overlap its neighbour's product (two device "
+                           "slots, three streams)",
+               "serial_ms_per_step": serial_ms,
+               "serial_value": whole_job_tflops(flop, 1, world, serial_ms / 1e3)}
         rc, site = g.gemm_f32_status(stream)
         if rc != 0:
             raise SystemExit("device error word %d in the e2e region" % site)

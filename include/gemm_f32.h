@@ -132,7 +132,34 @@ int gemm_f32_last_launches(void);
  * "none" (nothing launched).  Static string. */
 const char* gemm_f32_last_kernel(void);
 
-/* Frees the current device's workspaces after synchronising the device.
+/* C = A * B with A, B and C in HOST memory: copies A and B to the device,
+ * computes in `mode` (as gemm_f32_ex, no flags) and copies C back, all
+ * queued asynchronously.  For throughput, consecutive calls overlap: the
+ * library keeps per device two device-side slots (A, B and C buffers, grown
+ * on demand and freed by gemm_f32_release) used by alternate calls, and
+ * three internal streams (copy in, product, copy out), so one call's copies
+ * run while its neighbour's product does.  Events order every reuse of a
+ * slot.  Contract:
+ *   - A and B are read asynchronously, without waiting for work already
+ *     queued on `stream`: the host must have finished writing them, and must
+ *     not change them until `stream` has passed this call.
+ *   - `stream` waits for the copy of C: C holds the product once the work
+ *     queued on `stream` up to this call has completed (for example after
+ *     cudaStreamSynchronize or gemm_f32_status on `stream`).
+ *   - Pinned host memory (cudaMallocHost, cudaHostAlloc) gives asynchronous
+ *     copies at full link speed; pageable memory works but the runtime then
+ *     copies it through staging buffers, partly synchronously.
+ *   - C must not overlap A or B.  Calls from several host threads are
+ *     serialised per device.
+ * Returns 0, GEMM_F32_EINVAL (as gemm_f32_ex), GEMM_F32_EDEVICE or
+ * GEMM_F32_ELAUNCH (a copy, an event or an allocation failed).  The pages
+ * have no counterpart (their benchmark times device buffers); it is the
+ * host-to-host path a caller without device memory uses. */
+int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int mode,
+                  gemm_f32_stream_t stream);
+
+/* Frees the current device's workspaces (and gemm_f32_host's device slots)
+ * after synchronising the device.
  * Returns 0, or GEMM_F32_EDEVICE / GEMM_F32_ELAUNCH on a CUDA error. */
 int gemm_f32_release(void);
 

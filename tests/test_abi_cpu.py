@@ -22,7 +22,7 @@ def g():
 def test_header_declares_the_entry_points(g):
     names = g.declared_symbols()
     assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status", "gemm_f32_ladder",
-                            "gemm_f32_general",
+                            "gemm_f32_general", "gemm_f32_host",
                             "gemm_f32_last_kernel", "gemm_f32_last_launches", "gemm_f32_noalloc",
                             "gemm_f32_release",
                             "gemm_f32_version"])
@@ -108,6 +108,17 @@ def _with(**kw):
 ])
 def test_general_rejects_malformed_requests_on_the_host(g, args):
     assert g.gemm_f32_general(*args) == g.GEMM_F32_EINVAL
+    assert g.gemm_f32_last_launches() == 0
+
+
+@pytest.mark.parametrize("args,mode", [
+    ((FAKE_A, FAKE_B, FAKE_C, 4, 4, 4), 5),              # unknown mode
+    ((FAKE_A, FAKE_B, FAKE_C, 4, -4, 4), 0),             # negative N
+    ((FAKE_A, FAKE_B, 0, 4, 4, 4), 0),                   # null C
+    ((FAKE_A, FAKE_B, FAKE_A + 4, 4, 4, 4), 0),          # C overlaps A
+])
+def test_host_buffers_reject_malformed_requests(g, args, mode):
+    assert g.gemm_f32_host(*args, mode=mode) == g.GEMM_F32_EINVAL
     assert g.gemm_f32_last_launches() == 0
 
 
