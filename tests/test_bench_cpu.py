@@ -57,6 +57,23 @@ def test_reference_arm_line(capsys):
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
 
 
-def test_source_hash_is_stable():
-    assert bench.source_hash() == bench.source_hash()
-    assert len(bench.source_hash()) == 16
+def test_source_hash_is_stable_and_per_kernel():
+    for kernel in bench.KERNEL_SOURCES:
+        assert bench.source_hash(kernel) == bench.source_hash(kernel)
+        assert len(bench.source_hash(kernel)) == 16
+    assert bench.source_hash("tc_pair_kernel") != bench.source_hash("tc_gemm_kernel")
+
+
+def test_recorded_traffic_matches_the_current_sources():
+    # profiles/traffic.json is keyed by the kernel's own sources: a figure
+    # recorded for other sources reads as null
+    import json
+    import os
+    path = os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")
+    with open(path) as f:
+        table = json.load(f)
+    for key, rec in table.items():
+        kernel, config, mode = key.split("/")
+        want = rec["dram_bytes_per_launch"] if rec["source_sha"] == bench.source_hash(kernel) else None
+        assert bench.recorded_traffic(kernel, config, mode) == want
+    assert bench.recorded_traffic("tc_pair_kernel", "no-such-config", "tc3x") is None
