@@ -108,7 +108,12 @@ int gemm_f32(const float* A, const float* B, float* C, int M, int N, int K,
              gemm_f32_stream_t stream);
 
 /* C = A * B in an explicit mode with variant flags.  Returns 0 or a negative
- * code; GEMM_F32_EINVAL for an unknown mode or flag. */
+ * code; GEMM_F32_EINVAL for an unknown mode or flag.
+ * gemm_f32, gemm_f32_ex and gemm_f32_general may be captured into a CUDA
+ * graph on `stream` once a call of the same shape, mode and flags has run
+ * on the device outside the capture (that first call may allocate the
+ * split-tail workspace, which a capture must not); a replay computes with
+ * the captured pointers and whatever values they then hold. */
 int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K,
                 int mode, unsigned flags, gemm_f32_stream_t stream);
 
