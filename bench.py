@@ -397,10 +397,18 @@ def run_ours(args):
     else:
         peak = peaks["bf16_tflops"] * TF32_PER_BF16
         nprod = MODE_PRODUCTS[args.mode]
-        roof = {"bound": "tensor", "achieved": nprod * flop / t_kernel / 1e12, "peak": peak,
-                "unit": "TFLOP/s",
-                "peak_source": "%s bf16 burst x nominal tf32/bf16 ratio; achieved counts the %d "
-                               "tf32 products per fp32 product" % (peak_src, nprod)}
+        hbm = peaks.get("hbm_gbs")
+        # the binding roof: the larger of the two lower bounds on the time
+        if hbm and work_bytes / (hbm * 1e9) > nprod * flop / (peak * 1e12):
+            roof = {"bound": "hbm", "achieved": work_bytes / t_kernel / 1e9, "peak": hbm,
+                    "unit": "GB/s",
+                    "peak_source": "%s copy bandwidth; achieved = algorithmic bytes "
+                                   "4(MK + KN + MN) per launch / time" % peak_src}
+        else:
+            roof = {"bound": "tensor", "achieved": nprod * flop / t_kernel / 1e12, "peak": peak,
+                    "unit": "TFLOP/s",
+                    "peak_source": "%s bf16 burst x nominal tf32/bf16 ratio; achieved counts the %d "
+                                   "tf32 products per fp32 product" % (peak_src, nprod)}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["kernel"] = kernel
     roof["traffic"] = recorded_traffic(kernel, args.config, args.mode)
