@@ -64,6 +64,8 @@ using namespace gemm_f32_dev;
 namespace {
 
 constexpr int kTN = 128;                     // columns of C per tile = TMEM lanes = MMA M
+constexpr int kTNNarrow = 64;                // the same for N <= 64: an M = 64 MMA, whose
+                                             // rows sit in lanes 0-15 of each lane quarter
 constexpr int kWarps = 16;                   // see role table above
 constexpr int kThreads = kWarps * 32;
 constexpr int kEpilogueWarp0 = 4;
@@ -102,11 +104,11 @@ struct TcGeneral {
   int scale;             // C = alpha * acc (+ beta * C when beta != 0)
 };
 
-template <int TM, int BK, int NPROD>
+template <int TM, int BK, int NPROD, int TN = kTN>
 struct TcCfg {
   static constexpr int A_BYTES = TM * BK * 4;                       // A hi (TMA target)
   static constexpr int A_LO_BYTES = NPROD == 3 ? A_BYTES : 0;       // A lo
-  static constexpr int B_RAW_BYTES = BK * kTN * 4;                  // raw B tile [BK][128]
+  static constexpr int B_RAW_BYTES = BK * TN * 4;                   // raw B tile [BK][TN]
   static constexpr int STAGE_BYTES = A_BYTES + A_LO_BYTES + B_RAW_BYTES;
   static constexpr int NACC = TM == 256 ? 1 : 2;                    // accumulators in TMEM
   static constexpr int ACC_COLS = NACC * TM;
@@ -185,7 +187,7 @@ __device__ __forceinline__ bool epilogue_all(bool v) {
   return r != 0;
 }
 
-template <int TM, int BK, int NPROD, int LOAD>
+template <int TM, int BK, int NPROD, int LOAD, int TN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const TcParams p,
@@ -197,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool scale = !PLAIN_C && gp.scale;
   const int lda = GEN ? gp.lda : p.K, ldb = GEN ? gp.ldb : p.N;
   const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
-  using Cfg = TcCfg<TM, BK, NPROD>;
+  using Cfg = TcCfg<TM, BK, NPROD, TN>;
+  static_assert(TN == kTN || (TN == kTNNarrow && LOAD == kLoadTma), "narrow tiles: TMA only");
   constexpr int S = Cfg::STAGES;
   constexpr int NACC = Cfg::NACC;
   extern __shared__ uint8_t smem_dyn[];
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           armed |= 1u << s;
           last_ph = (last_ph & ~(1u << s)) | (ph << s);
           tma_load_2d(st, &tmA, full_bar(s), kt * BK, c.tm * TM);
-          tma_load_2d(st + Cfg::A_BYTES + Cfg::A_LO_BYTES, &tmB, full_bar(s), c.tn * kTN, kt * BK);
+          tma_load_2d(st + Cfg::A_BYTES + Cfg::A_LO_BYTES, &tmB, full_bar(s), c.tn * TN, kt * BK);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(kTN, TM, false, false);
+      constexpr uint32_t idesc = idesc_tf32(TN, TM, false, false);   // M = TN
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -345,7 +348,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
-    const int nl = q * 32 + lane;  // this thread's column within the tile
+    // this thread's column within the tile; with narrow tiles only lanes
+    // 0-15 of each quarter hold accumulator rows
+    const bool live = TN == kTN || lane < 16;
+    const int nl = TN == kTN ? q * 32 + lane : q * 16 + (lane & 15);
     int acc = 0;
     uint32_t acc_ph = 0;
     WorkList list(p);
@@ -355,24 +361,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * TM);
-      const int n = c.tn * kTN + nl;   // this thread's column of C
-      const bool n_ok = n < p.N;
+      const int n = c.tn * TN + nl;   // this thread's column of C
+      const bool n_ok = live && n < p.N;
       if (w.nseg > 1) {
         // part of a split tile: publish this partial; the CTA that publishes
         // last reduces the tile after its work list (see teardown)
         float* const mine = p.partials +
-                            (static_cast<size_t>(w.tail) * p.max_seg + w.seg) * (TM * kTN) + nl;
+                            (static_cast<size_t>(w.tail) * p.max_seg + w.seg) * (TM * TN) + nl;
 #pragma unroll 1
         for (int chunk = 0; chunk < TM / 32; ++chunk) {
           uint32_t v[32];
           tmem_ld_32cols(t_acc + chunk * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * kTN] = __uint_as_float(v[j]);
+          if (live)
+            for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * TN] = __uint_as_float(v[j]);
         }
         __threadfence();
         epilogue_sync();
-        if (nl == 0 && atomicAdd(p.counters + w.tail, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+        if (q == 0 && lane == 0 &&
+            atomicAdd(p.counters + w.tail, 1u) == static_cast<unsigned>(w.nseg - 1)) {
           // only the first and the last item of a CTA's share can be partial
           if (*pending_count < kMaxPending)
             pending[(*pending_count)++] = w;
@@ -416,9 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ transform
     constexpr int KH = BK / 2;                            // K rows of B per thread
     const int tt = threadIdx.x - kTransformWarp0 * 32;    // 0 .. 255
-    const int col = tt & 127;                             // = this thread's TMEM lane
+    const int q = (warp - kTransformWarp0) & 3;           // this warp's TMEM lane quarter
+    // this thread's column of the tile (its TMEM lane: 32q + lane); with
+    // narrow tiles lanes 16-31 of a quarter are not read by the MMA and carry
+    // a copy of lane - 16's column
+    const int col = TN == kTN ? q * 32 + lane : q * 16 + (lane & 15);
     const int kh0 = (tt >> 7) * KH;                       // first K row of its half
-    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(col & ~31) << 16);
+    const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -459,9 +471,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t* braw =
               reinterpret_cast<const uint32_t*>(st + Cfg::A_BYTES + Cfg::A_LO_BYTES);
 #pragma unroll
-          for (int k = 0; k < KH; ++k) split_operand<NPROD>(braw[(kh0 + k) * kTN + col], bh[k], bl[k]);
+          for (int k = 0; k < KH; ++k) split_operand<NPROD>(braw[(kh0 + k) * TN + col], bh[k], bl[k]);
         } else {
-          const int m0 = c.tm * TM, n0 = c.tn * kTN, k0 = kt * BK;
+          const int m0 = c.tm * TM, n0 = c.tn * TN, k0 = kt * BK;
           // This thread's loads for the stage are issued before any of them
           // is used (A in chunks of at most 16, the first with all of B), so
           // a few latencies cover the stage.
@@ -544,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkItem pw = pending[e];
       const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
       const float4* const parts = reinterpret_cast<const float4*>(
-          p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (TM * kTN));
-      constexpr int kVec = TM * kTN / 4;          // float4s per partial
+          p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (TM * TN));
+      constexpr int kVec = TM * TN / 4;           // float4s per partial
       constexpr int kPer = kVec / kThreads;       // per thread
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
@@ -570,8 +582,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kPer / 2; ++i) {
           const int f = threadIdx.x + (half * (kPer / 2) + i) * kThreads;  // float4 index
-          const int m = c.tm * TM + f / (kTN / 4);
-          const int n = c.tn * kTN + (f % (kTN / 4)) * 4;
+          const int m = c.tm * TM + f / (TN / 4);
+          const int n = c.tn * TN + (f % (TN / 4)) * 4;
           if (m < p.M) {
             float* dst = p.C + static_cast<size_t>(m) * static_cast<size_t>(ldc) + n;
             const float vals[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
@@ -621,12 +633,12 @@ bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, i
 
 constexpr int kMaxDevices = 64;
 
-template <int TM, int BK, int NPROD, int LOAD>
+template <int TM, int BK, int NPROD, int LOAD, int TN = kTN>
 int launch_one(const GemmArgs& g, const TcParams& p, const TcGeneral& gp, const CUtensorMap& ma,
                const CUtensorMap& mb, int grid, cudaStream_t stream) {
-  using Cfg = TcCfg<TM, BK, NPROD>;
+  using Cfg = TcCfg<TM, BK, NPROD, TN>;
   static std::atomic<unsigned long long> configured{0};  // bit per device
-  auto kern = tc_gemm_kernel<TM, BK, NPROD, LOAD>;
+  auto kern = tc_gemm_kernel<TM, BK, NPROD, LOAD, TN>;
   const unsigned long long bit = 1ull << (g.device % kMaxDevices);
   if (!(configured.load() & bit)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM) !=
@@ -641,26 +653,26 @@ int launch_one(const GemmArgs& g, const TcParams& p, const TcGeneral& gp, const 
   return GEMM_F32_OK;
 }
 
-template <int BK, int NPROD, int LOAD>
+template <int BK, int NPROD, int LOAD, int TN = kTN>
 int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const TcGeneral& gp,
               const CUtensorMap& ma, const CUtensorMap& mb, int grid, cudaStream_t stream) {
   switch (tm) {
-    case 64: return launch_one<64, BK, NPROD, LOAD>(g, p, gp, ma, mb, grid, stream);
-    case 128: return launch_one<128, BK, NPROD, LOAD>(g, p, gp, ma, mb, grid, stream);
-    default: return launch_one<256, BK, NPROD, LOAD>(g, p, gp, ma, mb, grid, stream);
+    case 64: return launch_one<64, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
+    case 128: return launch_one<128, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
+    default: return launch_one<256, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
   }
 }
 
 // Tile heights 64 and 128 are also built with BK = 32 for three products:
 // fewer, larger stages (the MMA thread's wait on a stage costs about as much
 // as the stage's MMAs at these heights).
-template <int NPROD, int LOAD>
+template <int NPROD, int LOAD, int TN = kTN>
 int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const TcGeneral& gp,
                  const CUtensorMap& ma, const CUtensorMap& mb, int grid, cudaStream_t stream) {
-  if (NPROD == 1) return launch_tm<32, 1, LOAD>(tm, g, p, gp, ma, mb, grid, stream);
-  if (bk == 16) return launch_tm<16, 3, LOAD>(tm, g, p, gp, ma, mb, grid, stream);
-  return tm == 64 ? launch_one<64, 32, 3, LOAD>(g, p, gp, ma, mb, grid, stream)
-                  : launch_one<128, 32, 3, LOAD>(g, p, gp, ma, mb, grid, stream);
+  if (NPROD == 1) return launch_tm<32, 1, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
+  if (bk == 16) return launch_tm<16, 3, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
+  return tm == 64 ? launch_one<64, 32, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream)
+                  : launch_one<128, 32, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
 }
 
 // The loader for a launch: TMA when the operands allow, else the staged
@@ -724,8 +736,12 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
 
 }  // namespace
 
-int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
-  if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
+// One launch with tiles `tn` columns wide (kTN, or kTNNarrow on the TMA
+// path only: returns kRetryWide, having launched nothing, when TMA cannot be
+// used after all).
+constexpr int kRetryWide = 1;
+
+int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launches) {
   *launches = 0;
   int bk = 0;
   TcParams p;
@@ -735,7 +751,7 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
-  p.tiles_n = ceil_div(g.N, kTN);
+  p.tiles_n = ceil_div(g.N, tn);
   p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
   const TcGeneral gp = general_of(g);
@@ -756,7 +772,7 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
     p.tiles_m = ceil_div(g.M, tm);
     const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
     if (tiles <= 0x7fffffffL)
-      ws_bytes = plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * kTN * sizeof(float));
+      ws_bytes = plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * tn * sizeof(float));
   }
   void* ws = nullptr;
   int must_clear = 0;
@@ -797,20 +813,38 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (tma) {
     tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, tm,
                     bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, g.ldb, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+          encode_2d(&mb, g.B, g.K, g.N, g.ldb, tn, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!tma) {
+    if (tn != kTN) return kRetryWide;
     memset(&ma, 0, sizeof(ma));
     memset(&mb, 0, sizeof(mb));
   }
-  const int rc = nprod == 3
-                     ? launch_loader<3>(tma, tm, bk, g, p, gp, ma, mb, grid, stream)
-                     : launch_loader<1>(tma, tm, bk, g, p, gp, ma, mb, grid, stream);
+  int rc;
+  if (tn == kTNNarrow)
+    rc = nprod == 3
+             ? launch_tm_bk<3, kLoadTma, kTNNarrow>(tm, bk, g, p, gp, ma, mb, grid, stream)
+             : launch_tm_bk<1, kLoadTma, kTNNarrow>(tm, bk, g, p, gp, ma, mb, grid, stream);
+  else
+    rc = nprod == 3 ? launch_loader<3>(tma, tm, bk, g, p, gp, ma, mb, grid, stream)
+                    : launch_loader<1>(tma, tm, bk, g, p, gp, ma, mb, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "tc_gemm_kernel";
   }
   return rc;
+}
+
+int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+  if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
+  // N <= 64: tiles 64 columns wide and an M = 64 MMA, so that no MMA work is
+  // spent on columns beyond N (measured on GB300: 65536 x 1024 x 64 had the
+  // tensor pipe 79 % busy with half of each M = 128 MMA discarded)
+  if (g.N <= kTNNarrow && !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && tma_addressable(g)) {
+    const int rc = launch_tc_tn(g, nprod, kTNNarrow, stream, launches);
+    if (rc != kRetryWide) return rc;
+  }
+  return launch_tc_tn(g, nprod, kTN, stream, launches);
 }
 
 // ---------------------------------------------------------------- fixed-scratch variant

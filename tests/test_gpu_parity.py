@@ -254,3 +254,25 @@ def test_last_kernel_names_the_path():
     assert g.gemm_f32_last_kernel() == "memset"
     assert g.gemm_f32_status(s) == (0, 0)
     assert not C.any()
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("shape", [(1000, 300, 64), (517, 129, 60), (64, 64, 4), (3000, 2048, 32),
+                                   (256, 4096, 64), (1, 40, 8)])
+def test_narrow_tiles(mode, shape):
+    # N <= 64 on the TMA path: 64-column tiles with an M = 64 MMA (rows in
+    # lanes 0-15 of each TMEM lane quarter); includes split tails (long K,
+    # few tiles) and N below the tile width
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "uniform", 700 + M + N)
+    Co, absAB = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode)
+    assert_close(C, Co, absAB, TOL[mode], "narrow %s/%s" % (shape, mode))
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+def test_narrow_tiles_integers_exact(mode):
+    A, B = workloads.make_inputs(777, 512, 64, "int8", 31)
+    Co, _ = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode)
+    assert_bit_exact(C, Co, "narrow int/%s" % mode)
