@@ -20,6 +20,16 @@
 // sits in memory, is the MMA's shared-memory B operand (N = TM).  The MMA
 // therefore accumulates the transposed tile, D[n][m] = C[m][n], which also
 // makes the epilogue's stores coalesced (lane t writes column n0 + t).
+// For N <= 64 the tile is 64 columns wide (TN = 64) and the MMA has M = 64,
+// whose rows live in lanes 0-15 of each 32-lane quarter (measured on GB300);
+// the transform and the epilogue follow that layout.
+//
+// Template parameters: tile height TM (256, 128, 64), stage depth BK (16,
+// 32), products NPROD (3: 3xTF32, 1: 1xTF32), operand loader LOAD (TMA;
+// per-thread loads of the plain product; per-thread loads of the general
+// form with row strides and stored transposes) and tile width TN.  The
+// general form's alpha / beta and strides arrive in a separate argument, so
+// that the plain product's code is left as it is.
 //
 // Roles inside one persistent CTA (one CTA per SM, 16 warps):
 //   warp 0        TMA producer: A tile [TM x BK] (swizzled) and B tile
@@ -31,7 +41,8 @@
 //                 (warps w and w+4 share TMEM lanes 32(w%4).., each taking
 //                 half of the tile's K rows).
 //                 On the staged path (operands TMA cannot address) these
-//                 warps load both tiles from global memory themselves.
+//                 warps load both tiles from global memory themselves, all of
+//                 a stage's loads issued before any is used.
 // Every role walks the same list of work items (below) and the same K-phase
 // count per item, so no role leaves a barrier phase unfinished (the
 // uniform-control rule of "Lesson 10", section 3).

@@ -16,13 +16,16 @@
 // tile from L2 and its shared memory serves half as many MMA operand bytes.
 //
 // Roles per CTA: warp 0 TMA producer (own halves); warp 1 TMEM allocation
-// (both CTAs, cta_group::2) and MMA issue (even CTA only); warps 2..3
-// forward finished stages to the even CTA; warps 4..7 epilogue (own
+// (both CTAs, cta_group::2) and MMA issue (even CTA only); warps 2, 3, 16
+// and 17 forward finished stages to the even CTA; warps 4..7 epilogue (own
 // accumulator half); warps 8..15 transform (own halves).  The even CTA's MMA
 // waits for both CTAs' stages (one cluster-scope arrive per CTA and stage)
 // and for both epilogues to drain the accumulator; its commits arrive on
 // both CTAs' barriers (multicast).  Waits are bounded as in
-// tc_gemm.cu; the split tail of the last wave works per CTA half.
+// tc_gemm.cu; the split tail of the last wave works per CTA half.  Where TMA
+// cannot address the operands the transform warps load them (LOAD selects
+// the plain product's loads or the general form's, as in tc_gemm.cu), with
+// stages 16 deep.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
