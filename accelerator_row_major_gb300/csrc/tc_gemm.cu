@@ -756,13 +756,18 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
 }
 
 // A shorter tile height that fills one wave without splitting K, when the
-// tallest tiles would leave SMs idle: measured on GB300, 1536^3 runs 33 us in
-// 144 tiles of 128 rows against 43 us in 72 tiles of 256 split along K.
+// tallest tiles would leave SMs idle and K is short enough that the split's
+// fixed cost matters: measured on GB300, 1536^3 runs 33 us in 144 tiles of
+// 128 rows against 43 us in 72 tiles of 256 split along K, while at K = 4096
+// the split of 256-row tiles wins (1536 x 1536 x 4096: 69 against 82 us).
 // Returns 0 when the usual choice stands (or a flag fixes the height).
+constexpr int kOneWaveMaxK = 2048;
+
 int one_wave_height(const GemmArgs& g, int tn) {
   if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
                  GEMM_F32_FLAG_ONE_TILE_PER_CTA))
     return 0;
+  if (g.K > kOneWaveMaxK) return 0;
   const long tiles_n = ceil_div(g.N, tn);
   if (g.M <= 128 || tiles_n * ceil_div(g.M, 256) >= g.num_sms) return 0;
   for (int tm : {128, 64}) {
@@ -881,6 +886,17 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
 
 int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
+  // One product does a third of the MMA work per stage, which leaves the
+  // single-CTA kernel's shared-memory traffic exposed; the pair kernel halves
+  // it and pays off at fewer tiles (measured on GB300: 2048^3 34.0 against
+  // 44.0 us, 2048 x 1024 x 4096 40.7 against 50.8 us), unless shorter tiles
+  // fill one wave (1536^3: 24.2 us single against 26.7 us pair).
+  const unsigned no_pair = GEMM_F32_FLAG_SINGLE_CTA | GEMM_F32_FLAG_TILE64 |
+                           GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
+                           GEMM_F32_FLAG_ONE_TILE_PER_CTA;
+  if (nprod == 1 && !(g.flags & no_pair) && g.M >= 256 && g.N >= 256 &&
+      !one_wave_height(g, kTN))
+    return launch_tc_pair(g, nprod, stream, launches);
   // N <= 64: tiles 64 columns wide and an M = 64 MMA, so that no MMA work is
   // spent on columns beyond N (measured on GB300: 65536 x 1024 x 64 had the
   // tensor pipe 79 % busy with half of each M = 128 MMA discarded)
