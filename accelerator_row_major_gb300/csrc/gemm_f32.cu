@@ -231,7 +231,9 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
   g.flags = flags;
   int launches = 0;
   int rc;
-  if (mode == GEMM_F32_MODE_FFMA)
+  if (flags == 0 && gemm_f32_impl::small_suits(g))
+    rc = gemm_f32_impl::launch_small(g, stream, &launches);
+  else if (mode == GEMM_F32_MODE_FFMA)
     rc = gemm_f32_impl::launch_ffma(g, stream, &launches);
   else
     rc = gemm_f32_impl::launch_tc(g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream, &launches);

@@ -67,6 +67,14 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
 // CUDA-core FFMA path.
 int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches);
 
+// Small products (at most kSmallMaxWork multiply-adds, K <= kSmallMaxK) on a
+// latency-lean CUDA-core kernel, in every mode: below these sizes launch and
+// pipeline set-up dominate the tensor-core kernels' time.
+constexpr long long kSmallMaxWork = 1LL << 23;
+constexpr int kSmallMaxK = 256;
+bool small_suits(const GemmArgs& g);
+int launch_small(GemmArgs& g, cudaStream_t stream, int* launches);
+
 // The pages' ladder kernels v0 .. v4 (step), for timing and teaching.
 int launch_ladder(GemmArgs& g, int step, cudaStream_t stream, int* launches);
 

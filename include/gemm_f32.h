@@ -101,6 +101,12 @@ enum gemm_f32_mode {
                                             after such a call.  Ignored by the
                                             FFMA mode, which has no waits.    */
 
+/* Small products: without flags, a product of at most 2^23 multiply-adds
+ * with K <= 256 runs in every mode on a CUDA-core kernel (fp32 fused
+ * multiply-adds, within every mode's bound): at these sizes launch and
+ * pipeline set-up, not arithmetic, set the time.  Any flag keeps the mode's
+ * own kernels. */
+
 /* C = A * B in the default mode (GEMM_F32_MODE_TC3X).  The environment
  * variable GEMM_F32_MODE ("tc3x", "ffma" or "tc1x"), read once per process,
  * changes the default.  Returns 0 or a negative GEMM_F32_E* code. */
@@ -132,7 +138,8 @@ int gemm_f32_last_launches(void);
 /* Name of the kernel the last successful call on this host thread launched:
  * "tc_pair_kernel" (tensor cores, 256 x 256 tiles on SM pairs),
  * "tc_gemm_kernel" (tensor cores, one SM per tile), "ffma_gemm_kernel",
- * "memset" (K == 0), "scale_window_kernel" (gemm_f32_general with
+ * "small_gemm_kernel" (small products), "memset" (K == 0),
+ * "scale_window_kernel" (gemm_f32_general with
  * alpha == 0 or K == 0), "ladder_v0" .. "ladder_v4" (gemm_f32_ladder) or
  * "none" (nothing launched).  Static string. */
 const char* gemm_f32_last_kernel(void);

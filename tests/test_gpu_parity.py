@@ -33,19 +33,28 @@ def small_problems():
     return out
 
 
+# Without flags, products below the small-problem size (c1, the edge sweep,
+# most degenerate shapes) run on the small CUDA-core kernel; FLAG_SINGLE
+# keeps them on the mode's own kernels (the tensor-core single-CTA kernel,
+# or the FFMA kernel), so both are checked.
+SMALL_OR_OWN = [0, FLAG_SINGLE]
+
+
+@pytest.mark.parametrize("flags", SMALL_OR_OWN)
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("name", ["c1", "c2", "c3"])
-def test_small_configs_within_tolerance(small_problems, name, mode):
+def test_small_configs_within_tolerance(small_problems, name, mode, flags):
     A, B, Co, absAB = small_problems[name]
-    C, _ = run_abi(A, B, mode)
-    assert_close(C, Co, absAB, TOL[mode], "%s/%s" % (name, mode))
+    C, _ = run_abi(A, B, mode, flags)
+    assert_close(C, Co, absAB, TOL[mode], "%s/%s/%#x" % (name, mode, flags))
 
 
+@pytest.mark.parametrize("flags", SMALL_OR_OWN)
 @pytest.mark.parametrize("mode", MODES)
-def test_integer_config_bit_exact(small_problems, mode):
+def test_integer_config_bit_exact(small_problems, mode, flags):
     A, B, Co, _ = small_problems["c1int"]
-    C, _ = run_abi(A, B, mode)
-    assert_bit_exact(C, Co, "c1int/%s" % mode)
+    C, _ = run_abi(A, B, mode, flags)
+    assert_bit_exact(C, Co, "c1int/%s/%#x" % (mode, flags))
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -96,13 +105,14 @@ def _edge_cases(seed, count):
     return sorted(cases)
 
 
+@pytest.mark.parametrize("flags", SMALL_OR_OWN)
 @pytest.mark.parametrize("mode", MODES)
-def test_edge_sweep(mode):
+def test_edge_sweep(mode, flags):
     for (M, K, N) in _edge_cases(5 + MODES.index(mode), 40):
         A, B = workloads.make_inputs(M, K, N, "uniform", M * 7 + K * 3 + N)
         Co, absAB = oracle_full(A, B)
-        C, _ = run_abi(A, B, mode)
-        assert_close(C, Co, absAB, TOL[mode], "edge %dx%dx%d/%s" % (M, K, N, mode))
+        C, _ = run_abi(A, B, mode, flags)
+        assert_close(C, Co, absAB, TOL[mode], "edge %dx%dx%d/%s/%#x" % (M, K, N, mode, flags))
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -123,26 +133,28 @@ def test_k_zero_writes_zeros(mode):
     assert C.shape == (70, 90) and not C.any()
 
 
+@pytest.mark.parametrize("flags", SMALL_OR_OWN)
 @pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("shape", [(1, 1, 1), (1, 513, 300), (300, 513, 1), (1, 1, 4096),
                                    (129, 1, 257), (2, 3000, 2)])
-def test_degenerate_shapes(mode, shape):
+def test_degenerate_shapes(mode, shape, flags):
     M, K, N = shape
     A, B = workloads.make_inputs(M, K, N, "normal", sum(shape))
     Co, absAB = oracle_full(A, B)
-    C, _ = run_abi(A, B, mode)
-    assert_close(C, Co, absAB, TOL[mode], "degenerate %s/%s" % (shape, mode))
+    C, _ = run_abi(A, B, mode, flags)
+    assert_close(C, Co, absAB, TOL[mode], "degenerate %s/%s/%#x" % (shape, mode, flags))
 
 
-def test_closed_forms_on_gpu():
+@pytest.mark.parametrize("flags", SMALL_OR_OWN)
+def test_closed_forms_on_gpu(flags):
     # A = I gives B exactly in every mode for TF32-exact values; ones give
     # column sums of small integers exactly
     n = 200
     B = workloads.make_inputs(1, n, 150, "int8", 3)[1]
     for mode in MODES:
-        C, _ = run_abi(np.eye(n, dtype=np.float32), B, mode)
+        C, _ = run_abi(np.eye(n, dtype=np.float32), B, mode, flags)
         assert_bit_exact(C, B, "identity/%s" % mode)
-        C, _ = run_abi(np.ones((33, n), np.float32), B, mode)
+        C, _ = run_abi(np.ones((33, n), np.float32), B, mode, flags)
         assert_bit_exact(C, np.broadcast_to(B.sum(axis=0, dtype=np.float64).astype(np.float32), (33, 150)),
                          "ones/%s" % mode)
 
@@ -252,6 +264,15 @@ def test_last_kernel_names_the_path():
         assert g.gemm_f32_last_kernel() == want, (mode, flags)
     assert g.gemm_f32_ex(A, B, C, 4096, 4096, 0, "tc3x", 0, s) == 0
     assert g.gemm_f32_last_kernel() == "memset"
+    # small products take the small CUDA-core kernel in every mode, unless a
+    # flag asks for the mode's own kernels
+    for mode in MODES:
+        assert g.gemm_f32_ex(A, B, C, 100, 70, 37, mode, 0, s) == 0
+        assert g.gemm_f32_last_kernel() == "small_gemm_kernel", mode
+    assert g.gemm_f32_ex(A, B, C, 100, 70, 37, "tc3x", FLAG_SINGLE, s) == 0
+    assert g.gemm_f32_last_kernel() == "tc_gemm_kernel"
+    assert g.gemm_f32_ex(A, B, C, 1000, 1000, 100, "tc3x", 0, s) == 0
+    assert g.gemm_f32_last_kernel() == "tc_gemm_kernel"
     assert g.gemm_f32_status(s) == (0, 0)
     assert not C.any()
 
