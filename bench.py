@@ -62,6 +62,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the one-line benchmark: every problem of workloads.py in every "
+                         "mode, warm and cold L2, mean and median, and the pages' statistic (one "
+                         "JSON line per row, then a table on stderr)")
     ap.add_argument("--ladder", action="store_true",
                     help="instead of the one-line benchmark: time the pages' kernels v0..v4, this "
                          "library's modes and torch.matmul on the pages' two sizes (one JSON line per "
@@ -525,8 +529,81 @@ def run_ladder(args):
     return 0
 
 
+def run_sweep(args):
+    """Every problem in every mode, as the measurement plan asks: warm L2
+    (the same inputs back to back, as on the pages) and cold L2 (a buffer
+    twice the L2 size written between calls), each call timed with CUDA
+    events on the launching stream after 3 warm-up calls; mean and median
+    over at least 20 calls, and the pages' own statistic (one warm-up, then
+    the mean of 10 calls; "LeetGPU problem 2", section "test environment and timing")."""
+    import torch
+
+    import accelerator_row_major_gb300 as g
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    reps = max(args.steps, 20)
+    rows = []
+    for cfg in ("c1", "c2", "c3", "c4", "c5a", "c5b", "c5c"):
+        p = workloads.CONFIGS[cfg]
+        A_h, B_h = workloads.problem_inputs(cfg)
+        A = torch.from_numpy(A_h).to(dev)
+        B = torch.from_numpy(B_h).to(dev)
+        C = torch.empty((p.M, p.N), dtype=torch.float32, device=dev)
+        flop = workloads.gemm_flops(p.M, p.N, p.K)
+        for mode in ("tc3x", "ffma", "tc1x"):
+            def call():
+                g.check(g.gemm_f32_ex(A, B, C, p.M, p.N, p.K, mode, 0, stream))
+            n = reps if flop < 1e12 or mode != "ffma" else max(3, reps // 10)
+
+            def timed(count, flush):
+                out = []
+                for _ in range(count):
+                    with torch.cuda.stream(stream):
+                        if flush:
+                            scratch.zero_()
+                        e0 = torch.cuda.Event(enable_timing=True)
+                        e1 = torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        call()
+                        e1.record(stream)
+                    e1.synchronize()
+                    out.append(e0.elapsed_time(e1))
+                return out
+            timed(3, False)
+            warm = timed(n, False)
+            cold = timed(n, True)
+            timed(1, False)
+            pages = statistics.fmean(timed(10, False))
+            kernel = g.gemm_f32_last_kernel()
+            row = {"config": cfg, "shape": [p.M, p.K, p.N], "mode": mode, "kernel": kernel,
+                   "warm_mean_ms": round(statistics.fmean(warm), 5),
+                   "warm_median_ms": round(statistics.median(warm), 5),
+                   "cold_mean_ms": round(statistics.fmean(cold), 5),
+                   "cold_median_ms": round(statistics.median(cold), 5),
+                   "pages_stat_ms": round(pages, 5), "calls": n,
+                   "tflops_warm_median": round(flop / statistics.median(warm) / 1e9, 2),
+                   "tflops_cold_median": round(flop / statistics.median(cold) / 1e9, 2)}
+            rows.append(row)
+            print(json.dumps(row), flush=True)
+        del A, B, C
+        torch.cuda.empty_cache()
+    sys.stderr.write("\n| problem | mode | kernel | warm median ms | cold median ms | pages' stat ms | TFLOPS warm / cold |\n"
+                     "|---|---|---|---|---|---|---|\n")
+    for r in rows:
+        sys.stderr.write("| %s %s | %s | %s | %.4f | %.4f | %.4f | %.1f / %.1f |\n" % (
+            r["config"], "x".join(str(v) for v in r["shape"]), r["mode"], r["kernel"],
+            r["warm_median_ms"], r["cold_median_ms"], r["pages_stat_ms"],
+            r["tflops_warm_median"], r["tflops_cold_median"]))
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.sweep:
+        return run_sweep(args)
     if args.ladder:
         return run_ladder(args)
     if args.impl == "reference":
