@@ -27,6 +27,8 @@ struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
   bool dirty = false;             // a kernel gave up on a wait since last use
+  void* pack = nullptr;           // repacked operands for the TMA path
+  size_t pack_bytes = 0;
 };
 
 struct DeviceState {
@@ -192,6 +194,29 @@ int zero_fill(float* C, int M, int N, cudaStream_t stream) {
 }
 
 }  // namespace
+
+void* gemm_f32_impl::acquire_pack_buffer(int device, cudaStream_t stream, size_t bytes) {
+  if (device < 0 || device >= kMaxDevices) return nullptr;
+  DeviceState& st = g_devices[device];
+  std::lock_guard<std::mutex> lock(st.ws_mu);
+  Workspace& w = st.ws[stream];
+  if (w.pack_bytes < bytes) {
+    if (w.pack) {
+      (void)cudaFree(w.pack);   // synchronises the device: no kernel still uses it
+      w.pack = nullptr;
+      w.pack_bytes = 0;
+    }
+    const size_t want = (bytes + (1u << 20) - 1) & ~static_cast<size_t>((1u << 20) - 1);
+    void* p = nullptr;
+    if (cudaMalloc(&p, want) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    w.pack = p;
+    w.pack_bytes = want;
+  }
+  return w.pack;
+}
 
 extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K, int mode,
                            unsigned flags, gemm_f32_stream_t stream_handle) {
@@ -568,8 +593,10 @@ extern "C" int gemm_f32_release(void) {
     (void)cudaGetLastError();
     rc = GEMM_F32_ELAUNCH;
   }
-  for (auto& kv : st->ws)
+  for (auto& kv : st->ws) {
     if (kv.second.ptr) (void)cudaFree(kv.second.ptr);
+    if (kv.second.pack) (void)cudaFree(kv.second.pack);
+  }
   st->ws.clear();
   host_pipe_free(g_pipes[dev]);
   return rc;

@@ -67,6 +67,23 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
 // CUDA-core FFMA path.
 int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches);
 
+// Operand repacking for the TMA path (pack.cu).  pack_operand writes op(X),
+// rows x cols (X itself, or the transpose of X stored cols x rows), row-major
+// with row stride ld_dst.  pack_for_tma rewrites g's A and B (pointers,
+// strides, transpose flags) to packed copies in the stream's pack buffer
+// when TMA cannot read them and the product has at least kPackMinWork
+// multiply-adds; it packs nothing otherwise (or without memory) and counts
+// its kernels in *launches.
+constexpr long long kPackMinWork = 1LL << 27;
+int pack_operand(const float* src, int rows, int cols, int ld_src, bool transposed, float* dst,
+                 int ld_dst, int num_sms, cudaStream_t stream);
+int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches);
+
+// The library's pack buffer for `stream` on `device`, grown to at least
+// `bytes` (1 MiB granules, cudaMalloc, which synchronises the device when it
+// grows); nullptr when the memory cannot be had.  Freed by gemm_f32_release.
+void* acquire_pack_buffer(int device, cudaStream_t stream, size_t bytes);
+
 // Small products (at most kSmallMaxWork multiply-adds, K <= kSmallMaxK) on a
 // latency-lean CUDA-core kernel, in every mode: below these sizes launch and
 // pipeline set-up dominate the tensor-core kernels' time.

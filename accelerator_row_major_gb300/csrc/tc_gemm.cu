@@ -884,7 +884,20 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
   return rc;
 }
 
+int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
+
 int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+  // operands TMA cannot read, in a large product: copy them first (measured
+  // on GB300, the staged loads run at about half the TMA path's speed)
+  int packs = 0;
+  const int prc = pack_for_tma(g, stream, &packs);
+  if (prc != GEMM_F32_OK) return prc;
+  const int rc = launch_tc_kernels(g, nprod, stream, launches);
+  if (rc == GEMM_F32_OK) *launches += packs;
+  return rc;
+}
+
+int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
   // One product does a third of the MMA work per stage, which leaves the
   // single-CTA kernel's shared-memory traffic exposed; the pair kernel halves

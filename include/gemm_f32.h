@@ -131,8 +131,9 @@ int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K,
 int gemm_f32_status(gemm_f32_stream_t stream, unsigned* site);
 
 /* Number of kernels the last successful call on this host thread launched
- * (0 for a no-op, 1 for a GEMM or for the K == 0 memset, 2 when a split-tail
- * workspace had to be re-zeroed first). */
+ * (0 for a no-op, 1 for a GEMM or for the K == 0 memset, plus one when a
+ * split-tail workspace had to be re-zeroed first and one per operand copied
+ * for the tensor-memory accelerator). */
 int gemm_f32_last_launches(void);
 
 /* Name of the kernel the last successful call on this host thread launched:
@@ -170,8 +171,11 @@ const char* gemm_f32_last_kernel(void);
 int gemm_f32_host(const float* A, const float* B, float* C, int M, int N, int K, int mode,
                   gemm_f32_stream_t stream);
 
-/* Frees the current device's workspaces (and gemm_f32_host's device slots)
- * after synchronising the device.
+/* Frees the current device's workspaces (split-tail partials, the copies of
+ * operands the tensor-memory accelerator cannot read — odd strides,
+ * unaligned bases or stored transposes in products of at least 2^27
+ * multiply-adds are copied once into aligned buffers first — and
+ * gemm_f32_host's device slots) after synchronising the device.
  * Returns 0, or GEMM_F32_EDEVICE / GEMM_F32_ELAUNCH on a CUDA error. */
 int gemm_f32_release(void);
 

@@ -297,3 +297,31 @@ def test_narrow_tiles_integers_exact(mode):
     Co, _ = oracle_full(A, B)
     C, _ = run_abi(A, B, mode)
     assert_bit_exact(C, Co, "narrow int/%s" % mode)
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("shape,offsets", [((1027, 1029, 1031), (0, 0, 0)),
+                                           ((1024, 1024, 1024), (1, 0, 0)),
+                                           ((2049, 511, 1536), (0, 0, 0))])
+def test_large_operands_tma_cannot_read_are_packed(mode, shape, offsets):
+    # odd strides or unaligned bases in a product of at least 2^27
+    # multiply-adds: the operands are copied into aligned buffers and the TMA
+    # path runs (two copies, then the product)
+    from tests._gpu import lib
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "uniform", 900 + M)
+    Co, absAB = oracle_full(A, B)
+    oa, ob, oc = offsets
+    C, _ = run_abi(A, B, mode, offset_a=oa, offset_b=ob, offset_c=oc)
+    assert_close(C, Co, absAB, TOL[mode], "packed %s/%s" % (shape, mode))
+    assert lib().gemm_f32_last_launches() >= 2
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+def test_forced_staged_large_misaligned(mode):
+    # the staged loads stay available for large products (FORCE_STAGED)
+    M, K, N = 1027, 1029, 1031
+    A, B = workloads.make_inputs(M, K, N, "uniform", 910)
+    Co, absAB = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode, FLAG_STAGED)
+    assert_close(C, Co, absAB, TOL[mode], "staged large/%s" % mode)
