@@ -174,11 +174,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-# the sources each kernel is compiled from (its own file and the shared headers)
+# the sources each kernel's device code comes from: its own file and the
+# device header (launch.h is host-side interface only)
 KERNEL_SOURCES = {
-    "tc_pair_kernel": ("tc_pair_gemm.cu", "device_common.cuh", "launch.h"),
-    "tc_gemm_kernel": ("tc_gemm.cu", "device_common.cuh", "launch.h"),
-    "ffma_gemm_kernel": ("ffma_gemm.cu", "device_common.cuh", "launch.h"),
+    "tc_pair_kernel": ("tc_pair_gemm.cu", "device_common.cuh"),
+    "tc_gemm_kernel": ("tc_gemm.cu", "device_common.cuh"),
+    "ffma_gemm_kernel": ("ffma_gemm.cu", "device_common.cuh"),
 }
 
 
