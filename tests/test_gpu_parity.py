@@ -325,3 +325,34 @@ def test_forced_staged_large_misaligned(mode):
     Co, absAB = oracle_full(A, B)
     C, _ = run_abi(A, B, mode, FLAG_STAGED)
     assert_close(C, Co, absAB, TOL[mode], "staged large/%s" % mode)
+
+
+@pytest.mark.parametrize("mode,flags", [("tc3x", 0), ("tc3x", FLAG_SINGLE), ("ffma", 0), ("tc1x", 0)])
+def test_output_beyond_two_to_the_31_elements(mode, flags):
+    # C with 49152^2 = 2.4e9 elements (9.7 GB): every kernel's index
+    # arithmetic must stay 64-bit where it addresses C; sampled entries,
+    # including the last rows and columns, against the oracle
+    import torch
+    from tests._gpu import lib
+    g = lib()
+    M = N = 49152
+    K = 32
+    A_h, B_h = workloads.make_inputs(M, K, N, "uniform", 1234)
+    dev = torch.device("cuda:0")
+    A = torch.from_numpy(A_h).to(dev)
+    B = torch.from_numpy(B_h).to(dev)
+    C = torch.full((M, N), float("nan"), device=dev)
+    s = torch.cuda.current_stream(dev)
+    g.check(g.gemm_f32_ex(A, B, C, M, N, K, mode, flags, s))
+    rc, site = g.gemm_f32_status(s)
+    assert rc == 0, site
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([rng.integers(0, M, 2000), [0, M - 1, M - 1, M - 2, 43690, 43691]])
+    cols = np.concatenate([rng.integers(0, N, 2000), [0, N - 1, 0, N - 1, 43690, 5]])
+    got = C[torch.from_numpy(rows).to(dev), torch.from_numpy(cols).to(dev)].cpu().numpy()
+    want, absAB = oracle.gemm_entries(A_h, B_h, rows, cols)
+    err = np.abs(got.astype(np.float64) - want)
+    assert not np.isnan(got).any()
+    assert (err <= TOL[mode] * absAB).all(), float((err / absAB).max())
+    del C
+    torch.cuda.empty_cache()
