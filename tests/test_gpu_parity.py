@@ -356,3 +356,45 @@ def test_output_beyond_two_to_the_31_elements(mode, flags):
     assert (err <= TOL[mode] * absAB).all(), float((err / absAB).max())
     del C
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x", "ffma"])
+@pytest.mark.parametrize("shape", [(16384, 8192, 128), (128, 131072, 128), (512, 65536, 512)])
+def test_split_tail_repeats_with_other_work_between(mode, shape):
+    """Shapes whose every tile is split along K (up to 64 CTAs on one tile):
+    twelve calls, each after a different split product on the same stream
+    has overwritten the shared partial-tile workspace, give bitwise the same
+    C, and sampled entries lie within the mode's bound of the oracle.  A
+    partial read before its writer published it, or a tile counter left
+    non-zero by an earlier call, would change some of them."""
+    import torch
+    from tests._gpu import lib
+    g = lib()
+    M, K, N = shape
+    dev = torch.device("cuda:0")
+    s = torch.cuda.current_stream(dev)
+    A, B = workloads.make_inputs(M, K, N, "normal", 7 + M + N)
+    dA, dB = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+    dC = torch.empty(M, N, dtype=torch.float32, device=dev)
+    others = []
+    for (m, k, n), seed in (((1024, 8192, 512), 3), ((128, 65536, 256), 4)):
+        oA, oB = workloads.make_inputs(m, k, n, "uniform", seed)
+        others.append((torch.from_numpy(oA).to(dev), torch.from_numpy(oB).to(dev),
+                       torch.empty(m, n, dtype=torch.float32, device=dev), m, n, k))
+    code = {"tc3x": g.MODE_TC3X, "tc1x": g.MODE_TC1X, "ffma": g.MODE_FFMA}[mode]
+    first = None
+    for it in range(12):
+        oA, oB, oC, m, n, k = others[it % 2]
+        assert g.gemm_f32_ex(oA, oB, oC, m, n, k, code, 0, s) == g.GEMM_F32_OK
+        assert g.gemm_f32_ex(dA, dB, dC, M, N, K, code, 0, s) == g.GEMM_F32_OK
+        got = dC.cpu().numpy()
+        if first is None:
+            first = got.copy()
+        else:
+            assert np.array_equal(got.view(np.uint32), first.view(np.uint32)), "call %d differs" % it
+    st, site = g.gemm_f32_status(s)
+    assert st == g.GEMM_F32_OK, "device error word: site %d" % site
+    rows, cols = sample_indices(M, N, 600, 99)
+    vals, absv = oracle.gemm_entries(A, B, rows, cols)
+    assert_close(first[rows, cols][None, :], vals[None, :], absv[None, :], TOL[mode],
+                 "split repeats %s/%s" % (shape, mode))
