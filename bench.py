@@ -66,6 +66,11 @@ def parse_args(argv=None):
                     help="instead of the one-line benchmark: every problem of workloads.py in every "
                          "mode, warm and cold L2, mean and median, and the pages' statistic (one "
                          "JSON line per row, then a table on stderr)")
+    ap.add_argument("--oracle-table", action="store_true",
+                    help="instead of the one-line benchmark: time the CPU oracle on every problem "
+                         "of workloads.py with all host threads (and with one thread for the small "
+                         "ones), the host's core count and CPU model alongside (one JSON line per "
+                         "row, then a table on stderr); needs no GPU")
     ap.add_argument("--ladder", action="store_true",
                     help="instead of the one-line benchmark: time the pages' kernels v0..v4, this "
                          "library's modes and torch.matmul on the pages' two sizes (one JSON line per "
@@ -229,6 +234,67 @@ def oracle_sample(A, B, seconds: float):
     return {"value": tflops, "unit": "TFLOPS", "cores": oracle.max_threads(), "kind": "oracle",
             "sample": "first %d of %d rows of A times all of B (%dx%dx%d), fp64 accumulation plus "
                       "|A||B|, %.1f s" % (rows, M, rows, K, N, dt)}, rows
+
+
+def host_cpu():
+    """(logical cores, CPU model) of this host, from the OS."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key, _, val = line.partition(":")
+                key = key.strip().lower()
+                if key in ("model name", "cpu model", "hardware") and val.strip():
+                    model = val.strip()
+                    break
+                if key == "cpu part" and model == "unknown":
+                    model = "cpu part " + val.strip()
+    except OSError:
+        pass
+    return os.cpu_count() or 1, model
+
+
+# problems small enough to time single-threaded as well
+ORACLE_ONE_THREAD = ("c1", "c1int", "c2", "c3")
+# problems timed on a row sample (the full product would take minutes)
+ORACLE_SAMPLED = ("c5a",)
+
+
+def run_oracle_table(args):
+    """Wall time of the oracle on every problem (generation excluded)."""
+    import oracle
+    cores, model = host_cpu()
+    rows_out = []
+    for name in sorted(workloads.CONFIGS):
+        p = workloads.CONFIGS[name]
+        A, B = workloads.make_inputs(p.M, p.K, p.N, p.law, p.seed)
+        for threads in ((0, 1) if name in ORACLE_ONE_THREAD else (0,)):
+            used = oracle.max_threads() if threads == 0 else 1
+            if name in ORACLE_SAMPLED:
+                base, rows = oracle_sample(A, B, args.cpu_seconds)
+                tflops, what = base["value"], base["sample"]
+                seconds = workloads.gemm_flops(p.M, p.N, p.K) / (tflops * 1e12)
+                kind = "projected from the sample"
+            else:
+                oracle.gemm(A[:1], B, threads)          # page in and load the library
+                t0 = time.perf_counter()
+                oracle.gemm(A, B, threads)
+                seconds = time.perf_counter() - t0
+                tflops = workloads.gemm_flops(p.M, p.N, p.K) / seconds / 1e12
+                what, kind = "full product", "measured"
+            row = {"oracle_table": name, "M": p.M, "K": p.K, "N": p.N, "threads": used,
+                   "seconds": seconds, "tflops": tflops, "timing": kind, "what": what,
+                   "host_cores": cores, "cpu_model": model}
+            rows_out.append(row)
+            print(json.dumps(row), flush=True)
+    print("host: %d cores, %s" % (cores, model), file=sys.stderr)
+    print("%-6s %-22s %7s %12s %10s  %s" % ("config", "M x K x N", "threads", "seconds", "TFLOPS",
+                                            "timing"), file=sys.stderr)
+    for r in rows_out:
+        print("%-6s %-22s %7d %12.4f %10.4f  %s" % (r["oracle_table"], "%dx%dx%d" % (r["M"], r["K"], r["N"]),
+                                                   r["threads"], r["seconds"], r["tflops"], r["timing"]),
+              file=sys.stderr)
+    return 0
 
 
 def run_reference(args):
@@ -603,6 +669,8 @@ def run_sweep(args):
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.oracle_table:
+        return run_oracle_table(args)
     if args.sweep:
         return run_sweep(args)
     if args.ladder:

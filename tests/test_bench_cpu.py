@@ -77,3 +77,22 @@ def test_recorded_traffic_matches_the_current_sources():
         want = rec["dram_bytes_per_launch"] if rec["source_sha"] == bench.source_hash(kernel) else None
         assert bench.recorded_traffic(kernel, config, mode) == want
     assert bench.recorded_traffic("tc_pair_kernel", "no-such-config", "tc3x") is None
+
+
+def test_oracle_table_rows(capsys, monkeypatch):
+    """--oracle-table: one JSON line per problem and thread count, with the
+    host's cores and CPU model (here restricted to the two tiny problems)."""
+    import workloads
+    small = {k: v for k, v in workloads.CONFIGS.items() if k in ("c1", "c1int")}
+    monkeypatch.setattr(workloads, "CONFIGS", small)
+    assert bench.main(["--oracle-table"]) == 0
+    rows = [json.loads(l) for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    import oracle
+    everyone = oracle.max_threads()
+    assert [(r["oracle_table"], r["threads"]) for r in rows] == \
+        [("c1", everyone), ("c1", 1), ("c1int", everyone), ("c1int", 1)]
+    cores, model = bench.host_cpu()
+    for r in rows:
+        assert r["seconds"] > 0 and r["tflops"] > 0 and r["timing"] == "measured"
+        assert (r["M"], r["K"], r["N"]) == (100, 37, 70)
+        assert r["host_cores"] == cores >= 1 and r["cpu_model"] == model
