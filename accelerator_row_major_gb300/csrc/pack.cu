@@ -7,7 +7,9 @@
 // of HBM traffic per element and pays for itself above a few hundred rows
 // and columns (the threshold sits in the launcher).
 //
-// pack_rows_kernel: dst[r][c] = src[r][c] (row strides ld_src, ld_dst).
+// pack_rows_kernel: dst[r][c] = src[r][c] (row strides ld_src, ld_dst); one
+// launch copies one or two such matrices (A and B of a product: one launch
+// instead of two, which is what a ragged mid-sized product notices).
 // pack_transpose_kernel: dst[r][c] = src[c][r], through 32 x 33 shared-memory
 // tiles so that both the reads and the writes are coalesced.
 // Columns c >= cols of dst are left as they are: TMA reads them as out of
@@ -25,14 +27,45 @@ namespace {
 
 constexpr int kTile = 32;
 
-__global__ void pack_rows_kernel(const float* __restrict__ src, int rows, int cols, long long ld_src,
-                                 float* __restrict__ dst, long long ld_dst) {
-  const long long total = static_cast<long long>(rows) * cols;
+struct RowCopy {
+  const float* src;
+  float* dst;
+  long long ld_src, ld_dst;
+  int rows, cols;
+};
+
+__global__ void pack_rows_kernel(RowCopy x, RowCopy y) {
+  const long long nx = static_cast<long long>(x.rows) * x.cols;
+  const long long total = nx + static_cast<long long>(y.rows) * y.cols;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = t / cols, c = t % cols;
-    dst[r * ld_dst + c] = __ldg(src + r * ld_src + c);
+    const bool in_x = t < nx;
+    const long long e = in_x ? t : t - nx;
+    const int cols = in_x ? x.cols : y.cols;
+    const long long r = e / cols, c = e % cols;
+    const float* const src = in_x ? x.src : y.src;
+    float* const dst = in_x ? x.dst : y.dst;
+    dst[r * (in_x ? x.ld_dst : y.ld_dst) + c] = __ldg(src + r * (in_x ? x.ld_src : y.ld_src) + c);
   }
+}
+
+int launch_rows(const RowCopy& x, const RowCopy& y, int num_sms, cudaStream_t stream) {
+  const long long total = static_cast<long long>(x.rows) * x.cols + static_cast<long long>(y.rows) * y.cols;
+  const long long want = (total + 255) / 256;
+  const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
+  pack_rows_kernel<<<grid, 256, 0, stream>>>(x, y);
+  return cudaGetLastError() == cudaSuccess ? GEMM_F32_OK : GEMM_F32_ELAUNCH;
+}
+
+RowCopy row_copy(const float* src, int rows, int cols, int ld_src, float* dst, int ld_dst) {
+  RowCopy m;
+  m.src = src;
+  m.dst = dst;
+  m.ld_src = ld_src;
+  m.ld_dst = ld_dst;
+  m.rows = rows;
+  m.cols = cols;
+  return m;
 }
 
 // block (32, 8): tile (blockIdx.y, blockIdx.x) of dst, rows r0.., cols c0..
@@ -58,10 +91,8 @@ int pack_operand(const float* src, int rows, int cols, int ld_src, bool transpos
                  int ld_dst, int num_sms, cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return GEMM_F32_OK;
   if (!transposed) {
-    const long long total = static_cast<long long>(rows) * cols;
-    const long long want = (total + 255) / 256;
-    const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-    pack_rows_kernel<<<grid, 256, 0, stream>>>(src, rows, cols, ld_src, dst, ld_dst);
+    return launch_rows(row_copy(src, rows, cols, ld_src, dst, ld_dst),
+                       row_copy(src, 0, 1, ld_src, dst, ld_dst), num_sms, stream);
   } else {
     const long long gy = (rows + kTile - 1) / kTile;
     if (gy > 65535) return GEMM_F32_EINVAL;
@@ -83,6 +114,19 @@ int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches) {
   const size_t b_bytes = pack_b ? static_cast<size_t>(g.K) * ldb * sizeof(float) : 0;
   float* const buf = static_cast<float*>(acquire_pack_buffer(g.device, stream, a_bytes + b_bytes));
   if (!buf) return GEMM_F32_OK;   // no memory for copies: the staged loads serve
+  float* const b_dst = buf + a_bytes / sizeof(float);
+  if (pack_a && pack_b && !g.trans_a && !g.trans_b) {
+    // both plain row copies: one launch
+    const int rc = launch_rows(row_copy(g.A, g.M, g.K, g.lda, buf, lda),
+                               row_copy(g.B, g.K, g.N, g.ldb, b_dst, ldb), g.num_sms, stream);
+    if (rc != GEMM_F32_OK) return rc;
+    g.A = buf;
+    g.lda = lda;
+    g.B = b_dst;
+    g.ldb = ldb;
+    ++*launches;
+    return GEMM_F32_OK;
+  }
   if (pack_a) {
     const int rc = pack_operand(g.A, g.M, g.K, g.lda, g.trans_a != 0, buf, lda, g.num_sms, stream);
     if (rc != GEMM_F32_OK) return rc;
@@ -92,10 +136,9 @@ int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches) {
     ++*launches;
   }
   if (pack_b) {
-    float* const dst = buf + a_bytes / sizeof(float);
-    const int rc = pack_operand(g.B, g.K, g.N, g.ldb, g.trans_b != 0, dst, ldb, g.num_sms, stream);
+    const int rc = pack_operand(g.B, g.K, g.N, g.ldb, g.trans_b != 0, b_dst, ldb, g.num_sms, stream);
     if (rc != GEMM_F32_OK) return rc;
-    g.B = dst;
+    g.B = b_dst;
     g.ldb = ldb;
     g.trans_b = 0;
     ++*launches;
