@@ -306,7 +306,7 @@ def test_narrow_tiles_integers_exact(mode):
 def test_large_operands_tma_cannot_read_are_packed(mode, shape, offsets):
     # odd strides or unaligned bases in a product of at least 2^27
     # multiply-adds: the operands are copied into aligned buffers and the TMA
-    # path runs (two copies, then the product)
+    # path runs (the copies, then the product)
     from tests._gpu import lib
     M, K, N = shape
     A, B = workloads.make_inputs(M, K, N, "uniform", 900 + M)
