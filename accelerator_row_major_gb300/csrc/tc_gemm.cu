@@ -22,7 +22,12 @@
 // makes the epilogue's stores coalesced (lane t writes column n0 + t).
 // For N <= 64 the tile is 64 columns wide (TN = 64) and the MMA has M = 64,
 // whose rows live in lanes 0-15 of each 32-lane quarter (measured on GB300);
-// the transform and the epilogue follow that layout.
+// the transform and the epilogue follow that layout.  Tiles of 64 rows with
+// three products read A hi and A lo as one operand of 128 rows (they are
+// adjacent in the stage), so each K step takes two N = 128 MMAs instead of
+// three N = 64 ones (an N = 64 MMA costs about 72 cycles in this kernel, an
+// N = 128 one about 73), and the lo x lo product comes along; the epilogue
+// adds the accumulator's hi-row and lo-row halves.
 //
 // Template parameters: tile height TM (256, 128, 64), stage depth BK (16,
 // 32), products NPROD (3: 3xTF32, 1: 1xTF32), operand loader LOAD (TMA;
@@ -122,8 +127,15 @@ struct TcCfg {
   static constexpr int A_LO_BYTES = NPROD == 3 ? A_BYTES : 0;       // A lo
   static constexpr int B_RAW_BYTES = BK * TN * 4;                   // raw B tile [BK][TN]
   static constexpr int STAGE_BYTES = A_BYTES + A_LO_BYTES + B_RAW_BYTES;
-  static constexpr int NACC = TM == 256 ? 1 : 2;                    // accumulators in TMEM
-  static constexpr int ACC_COLS = NACC * TM;
+  // Tiles of 64 rows with three products stack A hi and A lo (adjacent in
+  // the stage, rows 64..127 of one N = 128 operand): one MMA per B part and
+  // K step, 2 x N = 128 instead of 3 x N = 64, the fourth product lo x lo
+  // coming along for free.  The accumulator then has 2 TM columns (hi rows,
+  // lo rows), summed by the epilogue.
+  static constexpr bool STACK = TM == 64 && NPROD == 3;
+  static constexpr int ACC_W = STACK ? 2 * TM : TM;                 // columns per accumulator
+  static constexpr int NACC = (TM == 256 || STACK) ? 1 : 2;         // accumulators in TMEM
+  static constexpr int ACC_COLS = NACC * ACC_W;
   static constexpr int BT_COLS = BK * (NPROD == 3 ? 2 : 1);         // B^T hi (+ lo) per stage
   static constexpr int FIT_SMEM = (kSmemLimit - 2048) / STAGE_BYTES;
   static constexpr int FIT_TMEM = (kTmemCols - ACC_COLS) / BT_COLS;
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(TN, TM, false, false);   // M = TN
+      constexpr uint32_t idesc = idesc_tf32(TN, Cfg::ACC_W, false, false);   // M = TN
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -321,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && list.next(p, w)) {
         if (!mbar_wait(acce_bar(acc), acc_ph ^ 1u, p.err, kSiteMmaAccEmpty)) break;
         tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * TM);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::ACC_W);
         for (int kt = w.k0; kt < w.k1; ++kt) {
           if (!mbar_wait(ready_bar(s), ph, p.err, kSiteMmaReady)) {
             ok = false;
@@ -334,7 +346,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint64_t a_hi = smem_desc(st + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
             mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_hi, idesc, (kt > w.k0 || kk > 0) ? 1u : 0u);
-            if (NPROD == 3) {
+            if (Cfg::STACK) {
+              // a_hi spans [A hi; A lo] here: B_hi * both, then B_lo * both
+              mma_tf32_tmem_a(d_tmem, bt + BK + kk * 8, a_hi, idesc, 1u);
+            } else if (NPROD == 3) {
               const uint64_t a_lo =
                   smem_desc(st + Cfg::A_BYTES + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
               mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_lo, idesc, 1u);        // B_hi * A_lo
@@ -373,7 +388,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!epilogue_all(mbar_wait(accf_bar(acc), acc_ph, p.err, kSiteEpilogueFull))) break;
       tc_fence_after_sync();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * TM);
+                             static_cast<uint32_t>(acc * Cfg::ACC_W);
+      // rows chunk*32 .. +31 of the tile's accumulator (with STACK the sum of
+      // its hi-row and lo-row columns)
+      auto load_rows = [&](int chunk, uint32_t (&v)[32]) {
+        tmem_ld_32cols(t_acc + chunk * 32, v);
+        if constexpr (Cfg::STACK) {
+          uint32_t u[32];
+          tmem_ld_32cols(t_acc + TM + chunk * 32, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(u[j]));
+        } else {
+          tmem_wait_ld();
+        }
+      };
       const int n = c.tn * TN + nl;   // this thread's column of C
       const bool n_ok = live && n < p.N;
       if (w.nseg > 1) {
@@ -384,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int chunk = 0; chunk < TM / 32; ++chunk) {
           uint32_t v[32];
-          tmem_ld_32cols(t_acc + chunk * 32, v);
-          tmem_wait_ld();
+          load_rows(chunk, v);
           if (live) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * TN] = __uint_as_float(v[j]);
@@ -405,8 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
         for (int chunk = 0; chunk < TM / 32; ++chunk) {
           uint32_t v[32];
-          tmem_ld_32cols(t_acc + chunk * 32, v);
-          tmem_wait_ld();
+          load_rows(chunk, v);
           const int m0 = c.tm * TM + chunk * 32;
           if (n_ok) {
             float* dst = p.C + static_cast<size_t>(m0) * static_cast<size_t>(ldc) + n;
