@@ -773,7 +773,7 @@ int choose_tm(const GemmArgs& g, bool split_tail) {
   long best_cost = -1;
   int best = 256;
   const int tms[3] = {256, 128, 64};
-  const long eff_pct[3] = {100, 76, 43};
+  const long eff_pct[3] = {100, 81, 56};
   for (int i = 0; i < 3; ++i) {
     const long tiles = tn * ceil_div(g.M, tms[i]);
     const long rounds = (tiles + g.num_sms - 1) / g.num_sms;
