@@ -67,11 +67,15 @@ enum gemm_f32_mode {
                                kind::tf32): each operand is split into a
                                TF32 high part and a TF32 low part and three
                                products hi*hi + hi*lo + lo*hi are accumulated
-                               in fp32.  |C - exact| <= 1e-5 * (|A||B|)_ij.  */
+                               in fp32 (four, lo*lo too, in tiles of 64
+                               rows).  |C - exact| <= 1e-5 * (|A||B|)_ij.   */
     GEMM_F32_MODE_FFMA = 1, /* CUDA-core fp32 fused multiply-add, register
                                tiled.  Same 1e-5 bound.                     */
-    GEMM_F32_MODE_TC1X = 2  /* opt-in: one TF32 product on operands rounded
-                               to TF32 (nearest, ties away).  Bound 2e-3.   */
+    GEMM_F32_MODE_TC1X = 2  /* opt-in: one TF32 product; B rounded to TF32
+                               (nearest, ties away), A rounded the same way
+                               or, where the tensor-memory accelerator reads
+                               it, truncated by the tensor core (per-product
+                               error below 1.5e-3).  Bound 2e-3.            */
 };
 
 /* Flags of gemm_f32_ex (bitwise OR).  None changes the result beyond the
