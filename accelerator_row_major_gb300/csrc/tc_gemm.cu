@@ -717,7 +717,10 @@ int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const TcG
       if (bk == 16) return launch_tm<16, 1, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
     return launch_tm<32, 1, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
   }
-  if (bk == 16) return launch_tm<16, 3, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
+  // three products take 16-deep stages only with 256-row tiles (bk_for)
+  if (bk == 16)
+    return tm == 256 ? launch_one<256, 16, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream)
+                     : GEMM_F32_EINVAL;
   return tm == 64 ? launch_one<64, 32, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream)
                   : launch_one<128, 32, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
 }
