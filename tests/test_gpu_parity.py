@@ -9,8 +9,8 @@ import pytest
 
 import oracle
 import workloads
-from tests._gpu import (TOL, assert_bit_exact, assert_close, max_rel_err, oracle_full, run_abi,
-                        sample_indices)
+from tests._gpu import (TOL, assert_bit_exact, assert_close, lib, max_rel_err, oracle_full,
+                        run_abi, sample_indices)
 
 pytestmark = pytest.mark.gpu
 
@@ -289,6 +289,23 @@ def test_narrow_tiles(mode, shape):
     Co, absAB = oracle_full(A, B)
     C, _ = run_abi(A, B, mode)
     assert_close(C, Co, absAB, TOL[mode], "narrow %s/%s" % (shape, mode))
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("shape,flags", [((64, 65536, 64), 0), ((50, 20000, 40), 0),
+                                         ((517, 129, 60), FLAG_SINGLE), ((64, 64, 4), FLAG_SINGLE),
+                                         ((1, 40, 8), FLAG_SINGLE), ((1000, 300, 64), FLAG_TILE[64])])
+def test_narrow_tiles_of_64_rows(mode, shape, flags):
+    # 64-column tiles of 64 rows: with three products the stacked A hi / A lo
+    # operand on an M = 64 MMA (the accumulator's two halves summed by the
+    # epilogue); the small shapes are kept off the small-product kernel
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "normal", 710 + M + N)
+    Co, absAB = oracle_full(A, B)
+    C, outs = run_abi(A, B, mode, flags, repeats=2)
+    assert lib().gemm_f32_last_kernel() == "tc_gemm_kernel"
+    assert_close(C, Co, absAB, TOL[mode], "narrow 64-row %s/%s" % (shape, mode))
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
 
 
 @pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
