@@ -1,7 +1,7 @@
 #!/usr/bin/env python3
 """Throughput of the row-major FP32 GEMM on GB300; prints ONE JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5a]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 8192x8192x8192]
                     [--mode tc3x|ffma|tc1x] [--impl ours|reference]
 
 A step is one product C = A * B of the named problem (workloads.py) through
@@ -55,7 +55,7 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c5a", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--config", default="8192x8192x8192", choices=sorted(workloads.PROBLEMS))
     ap.add_argument("--mode", default="tc3x", choices=sorted(MODE_PRODUCTS))
     ap.add_argument("--flags", type=lambda s: int(s, 0), default=0, help="gemm_f32_ex flags (tuning)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU baseline sample")
@@ -255,9 +255,9 @@ def host_cpu():
 
 
 # problems small enough to time single-threaded as well
-ORACLE_ONE_THREAD = ("c1", "c1int", "c2", "c3")
+ORACLE_ONE_THREAD = ("100x37x70", "100x37x70-int", "1024x512x1024", "1001x513x777")
 # problems timed on a row sample (the full product would take minutes)
-ORACLE_SAMPLED = ("c5a",)
+ORACLE_SAMPLED = ("8192x8192x8192",)
 
 
 def run_oracle_table(args):
@@ -265,8 +265,8 @@ def run_oracle_table(args):
     import oracle
     cores, model = host_cpu()
     rows_out = []
-    for name in sorted(workloads.CONFIGS):
-        p = workloads.CONFIGS[name]
+    for name in workloads.PROBLEMS:
+        p = workloads.PROBLEMS[name]
         A, B = workloads.make_inputs(p.M, p.K, p.N, p.law, p.seed)
         for threads in ((0, 1) if name in ORACLE_ONE_THREAD else (0,)):
             used = oracle.max_threads() if threads == 0 else 1
@@ -302,7 +302,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    p = workloads.CONFIGS[args.config]
+    p = workloads.PROBLEMS[args.config]
     A, B = workloads.make_inputs(p.M, p.K, p.N, p.law, p.seed)
     budget = 150.0 / max(1, args.steps + args.warmup)
     _, rows = oracle_sample(A, B, min(budget, 5.0))
@@ -319,8 +319,8 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": "%s: %dx%dx%d (M,K,N) fp32 row-major, %s, seed %d" %
-                       (p.name, p.M, p.K, p.N, p.law, p.seed), "sample_rows": rows},
+            "config": {"workload": "%dx%dx%d (M,K,N) fp32 row-major, %s, seed %d" %
+                       (p.M, p.K, p.N, p.law, p.seed), "sample_rows": rows},
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": oracle.max_threads(),
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -344,7 +344,7 @@ def run_ours(args):
     build_mod.build()
     import accelerator_row_major_gb300 as g
 
-    p = workloads.CONFIGS[args.config]
+    p = workloads.PROBLEMS[args.config]
     M, K, N = p.M, p.K, p.N
     A_h, B_h = workloads.make_inputs(M, K, N, p.law, p.seed)
     stream = torch.cuda.Stream(device)
@@ -488,8 +488,8 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "%s: %dx%dx%d (M,K,N) fp32 row-major, %s, seed %d" %
-                       (p.name, M, K, N, p.law, p.seed), "M": M, "K": K, "N": N, "mode": args.mode,
+            "config": {"workload": "%dx%dx%d (M,K,N) fp32 row-major, %s, seed %d" %
+                       (M, K, N, p.law, p.seed), "M": M, "K": K, "N": N, "mode": args.mode,
                        "flags": args.flags,
                        "l2": "flushed between steps" if flush else "inputs larger than L2",
                        "parallelism": "replicas x%d" % world},
@@ -548,8 +548,8 @@ def run_ladder(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     rows = []
-    for cfg in ("c2", "c3"):
-        p = workloads.CONFIGS[cfg]
+    for cfg in ("1024x512x1024", "1001x513x777"):
+        p = workloads.PROBLEMS[cfg]
         A_h, B_h = workloads.problem_inputs(cfg)
         A = torch.from_numpy(A_h).to(dev)
         B = torch.from_numpy(B_h).to(dev)
@@ -613,8 +613,9 @@ def run_sweep(args):
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     reps = max(args.steps, 20)
     rows = []
-    for cfg in ("c1", "c2", "c3", "c4", "c5a", "c5b", "c5c"):
-        p = workloads.CONFIGS[cfg]
+    for cfg in ("100x37x70", "1024x512x1024", "1001x513x777", "4096x4096x4096", "8192x8192x8192",
+                "65536x1024x64", "64x4096x65536"):
+        p = workloads.PROBLEMS[cfg]
         A_h, B_h = workloads.problem_inputs(cfg)
         A = torch.from_numpy(A_h).to(dev)
         B = torch.from_numpy(B_h).to(dev)
@@ -660,8 +661,8 @@ def run_sweep(args):
     sys.stderr.write("\n| problem | mode | kernel | warm median ms | cold median ms | pages' stat ms | TFLOPS warm / cold |\n"
                      "|---|---|---|---|---|---|---|\n")
     for r in rows:
-        sys.stderr.write("| %s %s | %s | %s | %.4f | %.4f | %.4f | %.1f / %.1f |\n" % (
-            r["config"], "x".join(str(v) for v in r["shape"]), r["mode"], r["kernel"],
+        sys.stderr.write("| %s | %s | %s | %.4f | %.4f | %.4f | %.1f / %.1f |\n" % (
+            r["config"], r["mode"], r["kernel"],
             r["warm_median_ms"], r["cold_median_ms"], r["pages_stat_ms"],
             r["tflops_warm_median"], r["tflops_cold_median"]))
     return 0

@@ -46,7 +46,7 @@ def test_whole_job_tflops_single_rank():
 
 
 def test_reference_arm_line(capsys):
-    bench.main(["--impl", "reference", "--config", "c1", "--steps", "2", "--warmup", "1"])
+    bench.main(["--impl", "reference", "--config", "100x37x70", "--steps", "2", "--warmup", "1"])
     line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
     assert line["impl"] == "reference"
     for key in ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "higher_is_better",
@@ -83,14 +83,14 @@ def test_oracle_table_rows(capsys, monkeypatch):
     """--oracle-table: one JSON line per problem and thread count, with the
     host's cores and CPU model (here restricted to the two tiny problems)."""
     import workloads
-    small = {k: v for k, v in workloads.CONFIGS.items() if k in ("c1", "c1int")}
-    monkeypatch.setattr(workloads, "CONFIGS", small)
+    small = {k: v for k, v in workloads.PROBLEMS.items() if k in ("100x37x70", "100x37x70-int")}
+    monkeypatch.setattr(workloads, "PROBLEMS", small)
     assert bench.main(["--oracle-table"]) == 0
     rows = [json.loads(l) for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
     import oracle
     everyone = oracle.max_threads()
     assert [(r["oracle_table"], r["threads"]) for r in rows] == \
-        [("c1", everyone), ("c1", 1), ("c1int", everyone), ("c1int", 1)]
+        [("100x37x70", everyone), ("100x37x70", 1), ("100x37x70-int", everyone), ("100x37x70-int", 1)]
     cores, model = bench.host_cpu()
     for r in rows:
         assert r["seconds"] > 0 and r["tflops"] > 0 and r["timing"] == "measured"

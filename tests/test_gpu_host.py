@@ -36,7 +36,7 @@ def host_call(A, B, mode="tc3x", use_pinned=True):
 
 
 @pytest.mark.parametrize("mode", ["tc3x", "ffma", "tc1x"])
-@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+@pytest.mark.parametrize("name", ["100x37x70", "1024x512x1024", "1001x513x777"])
 def test_host_buffers_within_tolerance(name, mode):
     A, B = workloads.problem_inputs(name)
     Co, absAB = oracle_full(A, B)
@@ -45,16 +45,16 @@ def test_host_buffers_within_tolerance(name, mode):
 
 
 def test_host_buffers_pageable_memory():
-    A, B = workloads.problem_inputs("c3")
+    A, B = workloads.problem_inputs("1001x513x777")
     Co, absAB = oracle_full(A, B)
     C = host_call(A, B, "tc3x", use_pinned=False)
     assert_close(C, Co, absAB, TOL["tc3x"], "pageable")
 
 
 def test_host_buffers_integers_exact():
-    A, B = workloads.problem_inputs("c1int")
+    A, B = workloads.problem_inputs("100x37x70-int")
     Co, _ = oracle_full(A, B)
-    assert_bit_exact(host_call(A, B, "tc3x"), Co, "host c1int")
+    assert_bit_exact(host_call(A, B, "tc3x"), Co, "host 100x37x70-int")
 
 
 def test_host_k_zero_writes_zeros():
@@ -86,7 +86,7 @@ def test_queued_calls_keep_their_own_operands():
 
 def test_release_frees_the_slots_and_calls_still_work():
     g = lib()
-    A, B = workloads.problem_inputs("c2")
+    A, B = workloads.problem_inputs("1024x512x1024")
     host_call(A, B)
     assert g.gemm_f32_release() == 0
     Co, absAB = oracle_full(A, B)

@@ -18,14 +18,14 @@ STEPS = [0, 1, 2, 3, 4]
 @pytest.fixture(scope="module")
 def problems():
     out = {}
-    for name in ("c1", "c1int", "c2", "c3"):
+    for name in ("100x37x70", "100x37x70-int", "1024x512x1024", "1001x513x777"):
         A, B = workloads.problem_inputs(name)
         out[name] = (A, B) + oracle_full(A, B)
     return out
 
 
 @pytest.mark.parametrize("step", STEPS)
-@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+@pytest.mark.parametrize("name", ["100x37x70", "1024x512x1024", "1001x513x777"])
 def test_ladder_configs_within_tolerance(problems, name, step):
     A, B, Co, absAB = problems[name]
     C, _ = run_abi(A, B, ladder_step=step)
@@ -35,9 +35,9 @@ def test_ladder_configs_within_tolerance(problems, name, step):
 
 @pytest.mark.parametrize("step", STEPS)
 def test_ladder_integers_bit_exact(problems, step):
-    A, B, Co, _ = problems["c1int"]
+    A, B, Co, _ = problems["100x37x70-int"]
     C, _ = run_abi(A, B, ladder_step=step)
-    assert_bit_exact(C, Co, "c1int/v%d" % step)
+    assert_bit_exact(C, Co, "100x37x70-int/v%d" % step)
 
 
 @pytest.mark.parametrize("step", STEPS)
@@ -62,6 +62,6 @@ def test_ladder_k_zero_writes_zeros(step):
 
 @pytest.mark.parametrize("step", STEPS)
 def test_ladder_is_deterministic(problems, step):
-    A, B, _, _ = problems["c3"]
+    A, B, _, _ = problems["1001x513x777"]
     _, outs = run_abi(A, B, ladder_step=step, repeats=2)
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))

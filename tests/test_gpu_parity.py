@@ -26,14 +26,14 @@ FLAG_SINGLE = 0x800
 @pytest.fixture(scope="module")
 def small_problems():
     out = {}
-    for name in ("c1", "c1int", "c2", "c3"):
+    for name in ("100x37x70", "100x37x70-int", "1024x512x1024", "1001x513x777"):
         A, B = workloads.problem_inputs(name)
         C, absAB = oracle_full(A, B)
         out[name] = (A, B, C, absAB)
     return out
 
 
-# Without flags, products below the small-problem size (c1, the edge sweep,
+# Without flags, products below the small-problem size (100x37x70, the edge sweep,
 # most degenerate shapes) run on the small CUDA-core kernel; FLAG_SINGLE
 # keeps them on the mode's own kernels (the tensor-core single-CTA kernel,
 # or the FFMA kernel), so both are checked.
@@ -42,7 +42,7 @@ SMALL_OR_OWN = [0, FLAG_SINGLE]
 
 @pytest.mark.parametrize("flags", SMALL_OR_OWN)
 @pytest.mark.parametrize("mode", MODES)
-@pytest.mark.parametrize("name", ["c1", "c2", "c3"])
+@pytest.mark.parametrize("name", ["100x37x70", "1024x512x1024", "1001x513x777"])
 def test_small_configs_within_tolerance(small_problems, name, mode, flags):
     A, B, Co, absAB = small_problems[name]
     C, _ = run_abi(A, B, mode, flags)
@@ -52,9 +52,9 @@ def test_small_configs_within_tolerance(small_problems, name, mode, flags):
 @pytest.mark.parametrize("flags", SMALL_OR_OWN)
 @pytest.mark.parametrize("mode", MODES)
 def test_integer_config_bit_exact(small_problems, mode, flags):
-    A, B, Co, _ = small_problems["c1int"]
+    A, B, Co, _ = small_problems["100x37x70-int"]
     C, _ = run_abi(A, B, mode, flags)
-    assert_bit_exact(C, Co, "c1int/%s/%#x" % (mode, flags))
+    assert_bit_exact(C, Co, "100x37x70-int/%s/%#x" % (mode, flags))
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -71,7 +71,7 @@ def test_integer_k512_bit_exact(mode, flags):
 @pytest.mark.parametrize("tm", [64, 128, 256])
 @pytest.mark.parametrize("staged", [False, True])
 def test_every_tensor_variant_on_ragged_and_regular(small_problems, mode, tm, staged):
-    for name in ("c3", "c2"):
+    for name in ("1001x513x777", "1024x512x1024"):
         A, B, Co, absAB = small_problems[name]
         flags = FLAG_TILE[tm] | (FLAG_STAGED if staged else 0)
         C, _ = run_abi(A, B, mode, flags)
@@ -80,14 +80,14 @@ def test_every_tensor_variant_on_ragged_and_regular(small_problems, mode, tm, st
 
 @pytest.mark.parametrize("mode", MODES)
 def test_one_tile_per_cta_grid(small_problems, mode):
-    A, B, Co, absAB = small_problems["c3"]
+    A, B, Co, absAB = small_problems["1001x513x777"]
     C, _ = run_abi(A, B, mode, FLAG_ONE_TILE)
-    assert_close(C, Co, absAB, TOL[mode], "c3/one-tile/%s" % mode)
+    assert_close(C, Co, absAB, TOL[mode], "1001x513x777/one-tile/%s" % mode)
 
 
 @pytest.mark.parametrize("mode", MODES)
 def test_deterministic(small_problems, mode):
-    A, B, _, _ = small_problems["c3"]
+    A, B, _, _ = small_problems["1001x513x777"]
     _, outs = run_abi(A, B, mode, repeats=2)
     assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
 
@@ -159,7 +159,7 @@ def test_closed_forms_on_gpu(flags):
                          "ones/%s" % mode)
 
 
-@pytest.mark.parametrize("name", ["c4", "c5b", "c5c", "c5a"])
+@pytest.mark.parametrize("name", ["4096x4096x4096", "65536x1024x64", "64x4096x65536", "8192x8192x8192"])
 @pytest.mark.parametrize("mode", ["tc3x", "ffma"])
 def test_large_configs_sampled(name, mode):
     """Full-size problems in the default launch configuration: sampled
@@ -177,11 +177,11 @@ def test_large_configs_sampled(name, mode):
 
 
 def test_large_config_tc1x_sampled():
-    A, B = workloads.problem_inputs("c4")
+    A, B = workloads.problem_inputs("4096x4096x4096")
     C, _ = run_abi(A, B, "tc1x")
     rows, cols = sample_indices(A.shape[0], B.shape[1], 2000, 99)
     vals, absv = oracle.gemm_entries(A, B, rows, cols)
-    assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc1x"], "c4/tc1x")
+    assert_close(C[rows, cols][None, :], vals[None, :], absv[None, :], TOL["tc1x"], "4096x4096x4096/tc1x")
 
 
 @pytest.mark.parametrize("mode", ["tc3x", "tc1x", "ffma"])

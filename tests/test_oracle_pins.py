@@ -250,7 +250,7 @@ def test_random_tiny_against_exact_rationals(seed):
             assert abs(absAB[i, j] - float(qa)) <= K * 2.0 ** -52 * float(qa)
 
 
-@pytest.mark.parametrize("name", ["c3", "c4"])
+@pytest.mark.parametrize("name", ["1001x513x777", "4096x4096x4096"])
 def test_sampled_entries_within_exact_bound(name):
     """P-R: 100 random entries lie within 0.5 ulp + K*2^-53*absAB of exact."""
     A, B = workloads.problem_inputs(name)
@@ -273,7 +273,7 @@ def test_sampled_entries_within_exact_bound(name):
 
 
 def test_entries_equal_full_product_bitwise():
-    A, B = workloads.problem_inputs("c3")
+    A, B = workloads.problem_inputs("1001x513x777")
     C, absAB = oracle.gemm(A, B)
     rng = np.random.default_rng(9)
     rows = rng.integers(0, A.shape[0], 500)
@@ -285,7 +285,7 @@ def test_entries_equal_full_product_bitwise():
 
 # ----------------------------------------------------------------- integers
 def test_integer_problem_exact():
-    A, B = workloads.problem_inputs("c1int")
+    A, B = workloads.problem_inputs("100x37x70-int")
     assert A.min() >= -8 and A.max() <= 8 and B.min() >= -8 and B.max() <= 8
     C, absAB = oracle.gemm(A, B)
     Ci = A.astype(np.int64) @ B.astype(np.int64)

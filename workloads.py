@@ -5,17 +5,17 @@ holds none of the product's arithmetic: only random draws (numpy PCG64,
 one fresh generator per problem; A is drawn before B), the problem shapes,
 and the FLOP / byte counts used to turn times into throughput.
 
-Problem shapes (M, K, N), value laws and seeds:
-  c1      100 x 37 x 70      uniform[-1, 1)          seed 0
-  c1int   100 x 37 x 70      integers in [-8, 8]     seed 0  (bit-exact case)
-  c2      1024 x 512 x 1024  uniform[-1, 1)          seed 1  (the regular size
-          timed on "LeetGPU problem 2", section "benchmark summary")
-  c3      1001 x 513 x 777   uniform[-1, 1)          seed 2  (the ragged size
-          timed on the same page)
-  c4      4096^3             standard normal         seed 3
-  c5a     8192^3             standard normal         seed 4
-  c5b     65536 x 1024 x 64  standard normal         seed 4  (tall-skinny)
-  c5c     64 x 4096 x 65536  standard normal         seed 4  (short-wide)
+Problems, named by their shape M x K x N, with value laws and seeds:
+  100x37x70        uniform[-1, 1)          seed 0  (tiny, misaligned strides)
+  100x37x70-int    integers in [-8, 8]     seed 0  (bit-exact case)
+  1024x512x1024    uniform[-1, 1)          seed 1  (the regular size timed on
+                   "LeetGPU problem 2", section "benchmark summary")
+  1001x513x777     uniform[-1, 1)          seed 2  (the ragged size timed on
+                   the same page)
+  4096x4096x4096   standard normal         seed 3
+  8192x8192x8192   standard normal         seed 4
+  65536x1024x64    standard normal         seed 4  (tall-skinny)
+  64x4096x65536    standard normal         seed 4  (short-wide)
 """
 from __future__ import annotations
 
@@ -35,15 +35,15 @@ class Problem:
     note: str = ""
 
 
-CONFIGS = {
-    "c1": Problem("c1", 100, 37, 70, "uniform", 0, "tiny ragged, misaligned strides"),
-    "c1int": Problem("c1int", 100, 37, 70, "int8", 0, "integers in [-8, 8]: exact in fp32"),
-    "c2": Problem("c2", 1024, 512, 1024, "uniform", 1, "regular, tile aligned"),
-    "c3": Problem("c3", 1001, 513, 777, "uniform", 2, "ragged on every edge"),
-    "c4": Problem("c4", 4096, 4096, 4096, "normal", 3, "compute-bound square"),
-    "c5a": Problem("c5a", 8192, 8192, 8192, "normal", 4, "large compute-bound square"),
-    "c5b": Problem("c5b", 65536, 1024, 64, "normal", 4, "tall-skinny, bandwidth bound"),
-    "c5c": Problem("c5c", 64, 4096, 65536, "normal", 4, "short-wide, bandwidth bound"),
+PROBLEMS = {
+    "100x37x70": Problem("100x37x70", 100, 37, 70, "uniform", 0, "tiny ragged, misaligned strides"),
+    "100x37x70-int": Problem("100x37x70-int", 100, 37, 70, "int8", 0, "integers in [-8, 8]: exact in fp32"),
+    "1024x512x1024": Problem("1024x512x1024", 1024, 512, 1024, "uniform", 1, "regular, tile aligned"),
+    "1001x513x777": Problem("1001x513x777", 1001, 513, 777, "uniform", 2, "ragged on every edge"),
+    "4096x4096x4096": Problem("4096x4096x4096", 4096, 4096, 4096, "normal", 3, "compute-bound square"),
+    "8192x8192x8192": Problem("8192x8192x8192", 8192, 8192, 8192, "normal", 4, "large compute-bound square"),
+    "65536x1024x64": Problem("65536x1024x64", 65536, 1024, 64, "normal", 4, "tall-skinny, bandwidth bound"),
+    "64x4096x65536": Problem("64x4096x65536", 64, 4096, 65536, "normal", 4, "short-wide, bandwidth bound"),
 }
 
 
@@ -67,7 +67,7 @@ def make_inputs(M: int, K: int, N: int, law: str, seed: int):
 
 
 def problem_inputs(name: str):
-    p = CONFIGS[name]
+    p = PROBLEMS[name]
     return make_inputs(p.M, p.K, p.N, p.law, p.seed)
 
 
