@@ -72,11 +72,16 @@ def test_recorded_traffic_matches_the_current_sources():
     path = os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")
     with open(path) as f:
         table = json.load(f)
+    import workloads
     for key, rec in table.items():
         kernel, config, mode = key.split("/")
+        assert config in workloads.PROBLEMS and kernel in bench.KERNEL_SOURCES, key
         want = rec["dram_bytes_per_launch"] if rec["source_sha"] == bench.source_hash(kernel) else None
         assert bench.recorded_traffic(kernel, config, mode) == want
     assert bench.recorded_traffic("tc_pair_kernel", "no-such-config", "tc3x") is None
+    # the default bench line (tc3x on the largest square) has a current record
+    default = bench.parse_args([]).config
+    assert bench.recorded_traffic("tc_pair_kernel", default, "tc3x") is not None
 
 
 def test_oracle_table_rows(capsys, monkeypatch):
