@@ -20,9 +20,13 @@
 // sits in memory, is the MMA's shared-memory B operand (N = TM).  The MMA
 // therefore accumulates the transposed tile, D[n][m] = C[m][n], which also
 // makes the epilogue's stores coalesced (lane t writes column n0 + t).
-// For N <= 64 the tile is 64 columns wide (TN = 64) and the MMA has M = 64,
-// whose rows live in lanes 0-15 of each 32-lane quarter (measured on GB300);
-// the transform and the epilogue follow that layout.  Tiles of 64 rows with
+// For N <= 64 the tile is 64 columns wide (TN = 64).  With one product the
+// MMA has M = 64, whose rows live in lanes 0-15 of each 32-lane quarter
+// (measured on GB300), and the transform and the epilogue follow that
+// layout, as does the 256-row tile with three products; in shorter tiles
+// with three products B^T hi fills lanes 0-63 and B^T lo lanes 64-127 of an
+// M = 128 operand (two MMAs per K step, on A hi and on A lo), and the
+// epilogue adds lanes 64 + n to lanes n through shared memory.  Tiles of 64 rows with
 // three products read A hi and A lo as one operand of 128 rows (they are
 // adjacent in the stage), so each K step takes two N = 128 MMAs instead of
 // three N = 64 ones (an N = 64 MMA costs about 72 cycles in this kernel, an
@@ -132,16 +136,25 @@ struct TcCfg {
   // K step, 2 x N = 128 instead of 3 x N = 64, the fourth product lo x lo
   // coming along for free.  The accumulator then has 2 TM columns (hi rows,
   // lo rows), summed by the epilogue.
-  static constexpr bool STACK = TM == 64 && NPROD == 3;
+  // Narrow tiles (64 columns) of up to 128 rows with three products stack by
+  // lanes instead (at 256 rows the three M = 64 MMAs measured 1 % faster):
+  // B^T hi in TMEM lanes 0..63 and B^T lo in lanes 64..127 make one M = 128
+  // operand, so each K step takes two M = 128 MMAs (on A hi and on A lo)
+  // instead of three M = 64 ones, and the accumulator's lanes 64 + n (the
+  // B-lo sums) are added to lanes n by the epilogue through shared memory.
+  static constexpr bool LSTACK = TN == kTNNarrow && NPROD == 3 && TM <= 128;
+  static constexpr bool STACK = TM == 64 && NPROD == 3 && !LSTACK;
+  static constexpr int MMA_M = LSTACK ? 128 : TN;                   // TMEM lanes of the MMA
   static constexpr int ACC_W = STACK ? 2 * TM : TM;                 // columns per accumulator
   static constexpr int NACC = (TM == 256 || STACK) ? 1 : 2;         // accumulators in TMEM
   static constexpr int ACC_COLS = NACC * ACC_W;
-  static constexpr int BT_COLS = BK * (NPROD == 3 ? 2 : 1);         // B^T hi (+ lo) per stage
-  static constexpr int FIT_SMEM = (kSmemLimit - 2048) / STAGE_BYTES;
+  static constexpr int BT_COLS = (NPROD == 3 && !LSTACK) ? 2 * BK : BK;   // B^T columns per stage
+  static constexpr int XCHG_BYTES = LSTACK ? 64 * 33 * 4 : 0;       // epilogue exchange buffer
+  static constexpr int FIT_SMEM = (kSmemLimit - 2048 - XCHG_BYTES) / STAGE_BYTES;
   static constexpr int FIT_TMEM = (kTmemCols - ACC_COLS) / BT_COLS;
   static constexpr int S0 = FIT_SMEM < FIT_TMEM ? FIT_SMEM : FIT_TMEM;
   static constexpr int STAGES = S0 < 8 ? S0 : 8;
-  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 1024;
+  static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 1024 + XCHG_BYTES;
   static constexpr uint32_t A_SWZ_MASK = BK == 32 ? 7u : 3u;       // 128B or 64B swizzle
   static constexpr uint32_t A_LAYOUT = BK == 32 ? 2u : 4u;         // descriptor layout code
   static constexpr uint32_t A_SBO = BK == 32 ? 1024u : 512u;       // 8-row group stride
@@ -244,6 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // split tiles this CTA published last, reduced after the work list
   volatile int* const pending_count = reinterpret_cast<volatile int*>(base_ptr + (tmem_slot + 8u - base));
   WorkItem* const pending = reinterpret_cast<WorkItem*>(base_ptr + (tmem_slot + 16u - base));
+  // LSTACK: the epilogue's exchange of B-lo sums, [64 columns][33] floats
+  float* const xchg = reinterpret_cast<float*>(base_ptr + S * Cfg::STAGE_BYTES + 1024);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -323,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_tf32(TN, Cfg::ACC_W, false, false);   // M = TN
+      constexpr uint32_t idesc = idesc_tf32(Cfg::MMA_M, Cfg::ACC_W, false, false);
       int s = 0;
       uint32_t ph = 0;
       int acc = 0;
@@ -346,7 +361,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int kk = 0; kk < BK / 8; ++kk) {
             const uint64_t a_hi = smem_desc(st + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
             mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_hi, idesc, (kt > w.k0 || kk > 0) ? 1u : 0u);
-            if (Cfg::STACK) {
+            if (Cfg::LSTACK) {
+              // the TMEM operand holds B^T hi and lo in its two lane halves
+              const uint64_t a_lo =
+                  smem_desc(st + Cfg::A_BYTES + kk * 32, 16, Cfg::A_SBO, Cfg::A_LAYOUT);
+              mma_tf32_tmem_a(d_tmem, bt + kk * 8, a_lo, idesc, 1u);
+            } else if (Cfg::STACK) {
               // a_hi spans [A hi; A lo] here: B_hi * both, then B_lo * both
               mma_tf32_tmem_a(d_tmem, bt + BK + kk * 8, a_hi, idesc, 1u);
             } else if (NPROD == 3) {
@@ -376,10 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kEpilogueWarp0 && warp < kEpilogueWarp0 + 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // this warp may read TMEM lanes 32q .. 32q+31
-    // this thread's column within the tile; with narrow tiles only lanes
-    // 0-15 of each quarter hold accumulator rows
-    const bool live = TN == kTN || lane < 16;
-    const int nl = TN == kTN ? q * 32 + lane : q * 16 + (lane & 15);
+    // this thread's column within the tile; with narrow tiles of one product
+    // only lanes 0-15 of each quarter hold accumulator rows, with LSTACK
+    // quarters 2 and 3 hold the B-lo sums of quarters 0 and 1
+    const bool live = TN == kTN || (Cfg::LSTACK ? q < 2 : lane < 16);
+    const int nl = TN == kTN ? q * 32 + lane
+                             : (Cfg::LSTACK ? (q & 1) * 32 + lane : q * 16 + (lane & 15));
     int acc = 0;
     uint32_t acc_ph = 0;
     WorkList list(p);
@@ -400,6 +422,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(u[j]));
+        } else if constexpr (Cfg::LSTACK) {
+          tmem_wait_ld();
+          if (q >= 2) {
+            float* const row = xchg + ((q - 2) * 32 + lane) * 33;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) row[j] = __uint_as_float(v[j]);
+          }
+          epilogue_sync();
+          if (q < 2) {
+            const float* const row = xchg + (q * 32 + lane) * 33;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + row[j]);
+          }
+          epilogue_sync();   // the buffer is free for the next chunk
         } else {
           tmem_wait_ld();
         }
@@ -468,9 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tt = threadIdx.x - kTransformWarp0 * 32;    // 0 .. 255
     const int q = (warp - kTransformWarp0) & 3;           // this warp's TMEM lane quarter
     // this thread's column of the tile (its TMEM lane: 32q + lane); with
-    // narrow tiles lanes 16-31 of a quarter are not read by the MMA and carry
-    // a copy of lane - 16's column
-    const int col = TN == kTN ? q * 32 + lane : q * 16 + (lane & 15);
+    // narrow tiles of one product lanes 16-31 of a quarter are not read by
+    // the MMA and carry a copy of lane - 16's column; with LSTACK quarters 2
+    // and 3 carry the lo parts of quarters 0 and 1's columns
+    const int col = TN == kTN ? q * 32 + lane
+                              : (Cfg::LSTACK ? (q & 1) * 32 + lane : q * 16 + (lane & 15));
     const int kh0 = (tt >> 7) * KH;                       // first K row of its half
     const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     int s = 0;
@@ -565,8 +603,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t bt =
             lane_base + static_cast<uint32_t>(Cfg::ACC_COLS + s * Cfg::BT_COLS + kh0);
-        tmem_store_cols<KH>(bt, bh);
-        if (NPROD == 3) tmem_store_cols<KH>(bt + BK, bl);
+        if (Cfg::LSTACK) {
+          // lanes 0..63 take B^T hi, lanes 64..127 B^T lo (warp-uniform)
+          if (q >= 2)
+            tmem_store_cols<KH>(bt, bl);
+          else
+            tmem_store_cols<KH>(bt, bh);
+        } else {
+          tmem_store_cols<KH>(bt, bh);
+          if (NPROD == 3) tmem_store_cols<KH>(bt + BK, bl);
+        }
         tmem_wait_st();
         fence_proxy_async_smem();  // A hi/lo: generic-proxy writes -> tensor-core reads
         tc_fence_before_sync();
@@ -765,18 +811,21 @@ TcGeneral general_of(const GemmArgs& g) {
 // whole waves, so the most efficient height is used (256; 128 or 64 when M
 // is that small).  Without it (ONE_TILE_PER_CTA or NO_SPLIT_K), the height
 // whose schedule gives the busiest SM the least time: rounds of tiles x TM /
-// (relative efficiency), the efficiencies being the measured 8192^3
-// throughputs of TM = 128 and 64 relative to TM = 256.
-int choose_tm(const GemmArgs& g, bool split_tail) {
+// (relative efficiency), the efficiencies being measured throughputs of
+// TM = 128 and 64 relative to TM = 256: 8192^3 for tiles 128 columns wide,
+// 65536 x 1024 x 64 and 131072 x 1024 x 64 for narrow ones (where 128-row
+// tiles cost 4 % more per row than 256-row ones).
+int choose_tm(const GemmArgs& g, bool split_tail, int width) {
   if (g.flags & GEMM_F32_FLAG_TILE64) return 64;
   if (g.flags & GEMM_F32_FLAG_TILE128) return 128;
   if (g.flags & GEMM_F32_FLAG_TILE256) return 256;
   if (split_tail) return g.M <= 64 ? 64 : (g.M <= 128 ? 128 : 256);
-  const long tn = ceil_div(g.N, kTN);
+  const long tn = ceil_div(g.N, width);
   long best_cost = -1;
   int best = 256;
   const int tms[3] = {256, 128, 64};
-  const long eff_pct[3] = {100, 81, 56};
+  const long wide_pct[3] = {100, 81, 56}, narrow_pct[3] = {100, 96, 51};
+  const long* const eff_pct = width == kTN ? wide_pct : narrow_pct;
   for (int i = 0; i < 3; ++i) {
     const long tiles = tn * ceil_div(g.M, tms[i]);
     const long rounds = (tiles + g.num_sms - 1) / g.num_sms;
@@ -847,7 +896,7 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
   size_t ws_bytes = 0;
   const int one_wave_tm = one_wave_height(g, tn);
   if (!one_wave_tm && !(g.flags & (GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K))) {
-    tm = choose_tm(g, true);
+    tm = choose_tm(g, true, tn);
     bk = bk_for(nprod, tm, tma_ok);
     p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
@@ -859,7 +908,7 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
   int must_clear = 0;
   if (ws_bytes) ws = acquire_workspace(g.device, stream, ws_bytes, &must_clear);
   if (!ws) {
-    tm = one_wave_tm ? one_wave_tm : choose_tm(g, false);
+    tm = one_wave_tm ? one_wave_tm : choose_tm(g, false, tn);
     bk = bk_for(nprod, tm, tma_ok);
     p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
@@ -1002,7 +1051,7 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
   p.partials = nullptr;
   p.counters = nullptr;
   const bool tma_ok = tma_addressable(g);
-  int tm = choose_tm(g, true);
+  int tm = choose_tm(g, true, kTN);
   int bk = bk_for(nprod, tm, tma_ok);
   p.k_iters = ceil_div(g.K, bk);
   p.tiles_m = ceil_div(g.M, tm);
@@ -1024,7 +1073,7 @@ int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* la
     }
     *launches += 1;
   } else {
-    tm = choose_tm(g, false);
+    tm = choose_tm(g, false, kTN);
     bk = bk_for(nprod, tm, tma_ok);
     p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);

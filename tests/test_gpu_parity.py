@@ -294,11 +294,13 @@ def test_narrow_tiles(mode, shape):
 @pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
 @pytest.mark.parametrize("shape,flags", [((64, 65536, 64), 0), ((50, 20000, 40), 0),
                                          ((517, 129, 60), FLAG_SINGLE), ((64, 64, 4), FLAG_SINGLE),
-                                         ((1, 40, 8), FLAG_SINGLE), ((1000, 300, 64), FLAG_TILE[64])])
+                                         ((1, 40, 8), FLAG_SINGLE), ((1000, 300, 64), FLAG_TILE[64]),
+                                         ((1000, 300, 64), FLAG_TILE[128]), ((3000, 700, 20), FLAG_TILE[256])])
 def test_narrow_tiles_of_64_rows(mode, shape, flags):
-    # 64-column tiles of 64 rows: with three products the stacked A hi / A lo
-    # operand on an M = 64 MMA (the accumulator's two halves summed by the
-    # epilogue); the small shapes are kept off the small-product kernel
+    # 64-column tiles of every height, 64 rows mostly: with three products
+    # B^T hi and lo stacked by lanes into an M = 128 operand (the
+    # accumulator's lane halves summed through shared memory); the small
+    # shapes are kept off the small-product kernel
     M, K, N = shape
     A, B = workloads.make_inputs(M, K, N, "normal", 710 + M + N)
     Co, absAB = oracle_full(A, B)
