@@ -52,6 +52,15 @@ class GemmError(RuntimeError):
         self.code = code
 
 
+class UnitRates(ctypes.Structure):
+    """gemm_f32_unit_rates_t of include/gemm_f32.h."""
+    _fields_ = [("tf32_flop_per_clk_sm", ctypes.c_double),
+                ("tf32_pair_flop_per_clk_sm", ctypes.c_double),
+                ("ffma_flop_per_clk_sm", ctypes.c_double),
+                ("sm_mhz", ctypes.c_double),
+                ("num_sms", ctypes.c_int)]
+
+
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
         raise ImportError("libgemm_f32.so is not built (run accelerator_row_major_gb300.build.build())")
@@ -80,6 +89,8 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_release.restype = ci
     lib.gemm_f32_version.argtypes = []
     lib.gemm_f32_version.restype = ctypes.c_char_p
+    lib.gemm_f32_unit_rates.argtypes = [ctypes.POINTER(UnitRates)]
+    lib.gemm_f32_unit_rates.restype = ci
     return lib
 
 
@@ -188,6 +199,15 @@ def gemm_f32_last_kernel() -> str:
 def gemm_f32_release() -> int:
     """Frees the current device's workspaces (synchronises the device)."""
     return lib().gemm_f32_release()
+
+
+def gemm_f32_unit_rates() -> dict:
+    """Per-SM FLOP per clock of the tf32 tensor core (one SM, SM pairs) and
+    of the fp32 FFMA pipe, measured on the current device, with the SM clock
+    seen meanwhile; raises GemmError on failure."""
+    r = UnitRates()
+    check(lib().gemm_f32_unit_rates(ctypes.byref(r)), "gemm_f32_unit_rates")
+    return {name: getattr(r, name) for name, _ in UnitRates._fields_}
 
 
 def gemm_f32_version() -> str:

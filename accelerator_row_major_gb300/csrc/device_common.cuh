@@ -75,7 +75,57 @@ constexpr int kMinSplitIters = 64;       // least K iterations per CTA in the sp
 constexpr int kLoadStaged = 0;
 constexpr int kLoadTma = 1;
 constexpr int kLoadStagedGeneral = 2;
-constexpr size_t kCounterBytes = 4096;   // tile counters at the start of the workspace
+
+// Tile counters at the start of the workspace (kCounterBytes): one 64-bit
+// word per tail tile (two for CTA-pair tiles, one per half) holding
+// (generation << 32) | partials published, then, in the last 8 bytes, the
+// number of CTAs of the running launch that have finished and the
+// generation.  A launch with a split tail counts only arrivals made under
+// the current generation, and the last of its CTAs to finish moves the
+// generation on.  A launch that gave up on a bounded wait still finishes
+// every CTA, so the counts it left half done belong to an old generation
+// and the next launch on the workspace ignores them: no reset, on the host
+// or in a graph replay, is needed after a timeout.  (The generation is 32
+// bits: a stale count could only match again 2^32 split launches later.)
+constexpr size_t kCounterBytes = 4096;
+constexpr int kMaxTailWords = static_cast<int>((kCounterBytes - 64) / 8);   // 504
+
+struct TailControl {
+  unsigned done;   // CTAs of the running launch that have finished
+  unsigned gen;    // generation of the running launch
+};
+
+__host__ __device__ __forceinline__ TailControl* tail_control(void* counters) {
+  return reinterpret_cast<TailControl*>(static_cast<char*>(counters) + kCounterBytes - 8);
+}
+
+// Publishes one partial of a tail tile: returns how many partials of the
+// tile (this one included) have been published in the current launch.
+__device__ __forceinline__ unsigned tail_arrive(unsigned long long* words, int index) {
+  const unsigned gen = *reinterpret_cast<volatile unsigned*>(&tail_control(words)->gen);
+  unsigned long long* const w = words + index;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(w);
+  for (;;) {
+    const unsigned count =
+        static_cast<unsigned>(old >> 32) == gen ? static_cast<unsigned>(old) : 0u;
+    const unsigned long long want = (static_cast<unsigned long long>(gen) << 32) | (count + 1u);
+    const unsigned long long seen = atomicCAS(w, old, want);
+    if (seen == old) return count + 1u;
+    old = seen;
+  }
+}
+
+// Called once per CTA (one thread) after the CTA's last use of the tile
+// counters, by every CTA of a launch that has a split tail.
+__device__ __forceinline__ void tail_launch_done(void* counters) {
+  TailControl* const t = tail_control(counters);
+  __threadfence();
+  if (atomicAdd(&t->done, 1u) == gridDim.x - 1) {
+    t->done = 0u;
+    __threadfence();
+    atomicAdd(&t->gen, 1u);
+  }
+}
 
 // One unit of a CTA's work: K iterations [k0, k1) of one output tile.
 struct WorkItem {
@@ -143,7 +193,7 @@ struct WorkList {
 // the split needs, 0 when whole tiles are better (no split).
 template <class P>
 inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_bytes,
-                              int min_iters = kMinSplitIters) {
+                              int min_iters = kMinSplitIters, int words_per_tile = 1) {
   p.dp_tiles = static_cast<int>(tiles);
   p.sk_ctas = 0;
   p.sk_work = 0;
@@ -159,7 +209,7 @@ inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_by
     const int last = sk_owner((i + 1) * static_cast<long long>(p.k_iters) - 1, ctas, work);
     max_seg = std::max(max_seg, last - first + 1);
   }
-  if (max_seg == 1 || tail * sizeof(unsigned) > kCounterBytes) return 0;
+  if (max_seg == 1 || tail * words_per_tile > kMaxTailWords) return 0;
   p.dp_tiles = static_cast<int>(tiles - tail);
   p.sk_ctas = static_cast<int>(ctas);
   p.sk_work = work;

@@ -63,7 +63,7 @@ struct FfmaParams {
   long long sk_work;     // (tiles - dp_tiles) * k_iters
   int max_seg;           // most CTAs sharing one tail tile
   float* partials;       // [tail tile][max_seg][128][256] fp32
-  unsigned* counters;    // [tail tile]: partials written so far (zero between calls)
+  unsigned long long* counters;   // [tail tile]: generation and partials published
   unsigned* err;
 };
 
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
       __threadfence();
       __syncthreads();
       if (threadIdx.x == 0 &&
-          atomicAdd(p.counters + w.tail, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+          tail_arrive(p.counters, w.tail) == static_cast<unsigned>(w.nseg)) {
         // only the first and the last item of a CTA's share can be partial
         if (pending_count < kMaxPending)
           pending[pending_count++] = w;
@@ -351,9 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
         reduce_partials_general<kBM, kBN, kThreads, 8>(parts, pw.nseg, c.tm * kBM, c.tn * kBN,
                                                        p.M, p.N, p.C, gp.ldc, gp.scale, gp.alpha,
                                                        gp.beta);
-      if (threadIdx.x == 0) p.counters[pw.tail] = 0;   // ready for the next call
     }
   }
+  if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
 }
 
 constexpr int kMaxDevices = 64;
@@ -416,20 +416,12 @@ int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
     FfmaParams q = p;
     const size_t ws_bytes =
         plan_split_tail(q, tiles, g.num_sms, sizeof(float) * kBM * kBN, kMinSplitItersFfma);
-    int must_clear = 0;
-    void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes, &must_clear) : nullptr;
+    void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes) : nullptr;
     if (ws) {
       p = q;
       grid = g.num_sms;
-      p.counters = static_cast<unsigned*>(ws);
+      p.counters = static_cast<unsigned long long*>(ws);
       p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
-      if (must_clear) {
-        if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
-          (void)cudaGetLastError();
-          return GEMM_F32_ELAUNCH;
-        }
-        *launches += 1;
-      }
     }
   }
   // 16-byte copies: untransposed, strides a multiple of 4 floats, aligned

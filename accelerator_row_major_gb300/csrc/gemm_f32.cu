@@ -26,7 +26,6 @@ constexpr int kMaxDevices = 64;
 struct Workspace {
   void* ptr = nullptr;
   size_t bytes = 0;
-  bool dirty = false;             // a kernel gave up on a wait since last use
   void* pack = nullptr;           // repacked operands for the TMA path
   size_t pack_bytes = 0;
 };
@@ -36,6 +35,8 @@ struct DeviceState {
   int status = GEMM_F32_EDEVICE;  // GEMM_F32_OK once set up
   int num_sms = 0;
   unsigned* err = nullptr;        // device address of g_error_word
+  std::mutex fixed_mu;
+  void* fixed_scratch = nullptr;  // device address of gemm_f32_noalloc's array
   std::mutex ws_mu;
   std::unordered_map<cudaStream_t, Workspace> ws;  // one per stream
 };
@@ -46,7 +47,10 @@ thread_local const char* t_last_kernel = "none";
 
 // Set-up runs once per device, with that device current: checks it is an
 // sm_103 part, reads the SM count, takes the address of the error word and
-// clears it.
+// clears it, and looks up the address of gemm_f32_noalloc's fixed scratch
+// array (which, under lazy module loading, loads the module that holds it:
+// the array is placed here, at the library's first call on the device, not
+// inside a later gemm_f32_noalloc call).
 DeviceState* device_state(int* device_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -76,9 +80,18 @@ DeviceState* device_state(int* device_out) {
     }
     st.num_sms = sms;
     st.err = static_cast<unsigned*>(p);
+    st.fixed_scratch = gemm_f32_impl::fixed_scratch_address();   // retried if null
     st.status = GEMM_F32_OK;
   });
   return &st;
+}
+
+// The fixed scratch array's device address on the current device, looked up
+// again if the set-up could not get it (a failed lookup is not kept).
+void* fixed_scratch(DeviceState* st) {
+  std::lock_guard<std::mutex> lock(st->fixed_mu);
+  if (!st->fixed_scratch) st->fixed_scratch = gemm_f32_impl::fixed_scratch_address();
+  return st->fixed_scratch;
 }
 
 int default_mode() {
@@ -104,9 +117,7 @@ constexpr unsigned kKnownFlags = GEMM_F32_FLAG_FORCE_STAGED | GEMM_F32_FLAG_TILE
 
 }  // namespace
 
-void* gemm_f32_impl::acquire_workspace(int device, cudaStream_t stream, size_t bytes,
-                                       int* must_clear) {
-  *must_clear = 0;
+void* gemm_f32_impl::acquire_workspace(int device, cudaStream_t stream, size_t bytes) {
   if (device < 0 || device >= kMaxDevices) return nullptr;
   DeviceState& st = g_devices[device];
   std::lock_guard<std::mutex> lock(st.ws_mu);
@@ -130,11 +141,6 @@ void* gemm_f32_impl::acquire_workspace(int device, cudaStream_t stream, size_t b
     }
     w.ptr = p;
     w.bytes = want;
-    w.dirty = false;
-  }
-  if (w.dirty) {
-    *must_clear = 1;
-    w.dirty = false;
   }
   return w.ptr;
 }
@@ -549,7 +555,7 @@ extern "C" int gemm_f32_noalloc(const float* A, const float* B, float* C, int M,
   g.flags = 0;
   int launches = 0;
   const int rc = gemm_f32_impl::launch_tc_fixed_scratch(
-      g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, stream, &launches);
+      g, mode == GEMM_F32_MODE_TC1X ? 1 : 3, fixed_scratch(st), stream, &launches);
   if (rc == GEMM_F32_OK) {
     t_last_launches = launches;
     t_last_kernel = g.kernel;
@@ -574,10 +580,6 @@ extern "C" int gemm_f32_status(gemm_f32_stream_t stream_handle, unsigned* site) 
     return GEMM_F32_ELAUNCH;
   }
   if (site) *site = word;
-  if (word) {  // a kernel may have left split-tail counters half counted
-    std::lock_guard<std::mutex> lock(st->ws_mu);
-    for (auto& kv : st->ws) kv.second.dirty = true;
-  }
   return word ? GEMM_F32_ETIMEOUT : GEMM_F32_OK;
 }
 

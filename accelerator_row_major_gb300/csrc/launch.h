@@ -43,11 +43,11 @@ inline bool tma_addressable(const GemmArgs& g) {
 
 // The library's workspace for `stream` on `device` (one per device and
 // stream), grown to at least `bytes` with cudaMalloc when needed (which
-// synchronises the device) and zeroed when allocated.  *must_clear is set
-// when the caller must re-zero the split-tail counters before using it (a
-// kernel on this device gave up on a bounded wait since it was last used).
-// Returns nullptr if the memory cannot be had; the caller then does without.
-void* acquire_workspace(int device, cudaStream_t stream, size_t bytes, int* must_clear);
+// synchronises the device) and zeroed when allocated.  Its split-tail
+// counters stay valid from call to call, even after a kernel gave up on a
+// bounded wait (device_common.cuh).  Returns nullptr if the memory cannot be
+// had; the caller then does without.
+void* acquire_workspace(int device, cudaStream_t stream, size_t bytes);
 
 // Tensor-core path (tcgen05.mma kind::tf32).  nprod = 3 (split hi/lo, three
 // products) or 1 (operands rounded to TF32, one product).  Returns 0 or a
@@ -59,10 +59,15 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 bool tc_pair_suits(const GemmArgs& g);
 int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 
-// Tensor-core path whose split-tail scratch comes from a fixed array inside
-// the library (no allocation).  Returns GEMM_F32_ESCRATCH if the product
-// would need more than GEMM_F32_NOALLOC_SCRATCH_BYTES.
-int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
+// Tensor-core path on the single-CTA kernel whose split-tail scratch is the
+// fixed array inside the library at `scratch` (no allocation, no operand
+// packing).  Returns GEMM_F32_ESCRATCH if the product would need more than
+// GEMM_F32_NOALLOC_SCRATCH_BYTES, GEMM_F32_EDEVICE if `scratch` is null.
+// fixed_scratch_address() gives the array's device address on the current
+// device (nullptr if the runtime cannot give it).
+int launch_tc_fixed_scratch(GemmArgs& g, int nprod, void* scratch, cudaStream_t stream,
+                            int* launches);
+void* fixed_scratch_address();
 
 // CUDA-core FFMA path.
 int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches);

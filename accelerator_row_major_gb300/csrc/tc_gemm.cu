@@ -110,7 +110,7 @@ struct TcParams {
   long long sk_work;     // (tiles - dp_tiles) * k_iters
   int max_seg;           // most CTAs sharing one tail tile
   float* partials;       // [tail tile][max_seg][TM][128] fp32
-  unsigned* counters;    // [tail tile]: partials written so far (zero between calls)
+  unsigned long long* counters;   // [tail tile]: generation and partials published
   int drop_first_copy;   // testing only: CTA 0 skips its first copy
   unsigned* err;
 };
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         epilogue_sync();
         if (q == 0 && lane == 0 &&
-            atomicAdd(p.counters + w.tail, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+            tail_arrive(p.counters, w.tail) == static_cast<unsigned>(w.nseg)) {
           // only the first and the last item of a CTA's share can be partial
           if (*pending_count < kMaxPending)
             pending[(*pending_count)++] = w;
@@ -682,9 +682,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (threadIdx.x == 0) p.counters[pw.tail] = 0;   // ready for the next call
     }
   }
+  if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
 }
 
 // ---------------------------------------------------------------- host side
@@ -862,12 +862,22 @@ int one_wave_height(const GemmArgs& g, int tn) {
 
 }  // namespace
 
+// Where a launch's split-tail scratch comes from: the library's workspace
+// for the stream (allocated on first use), or, for gemm_f32_noalloc, a
+// fixed region that is never grown.
+struct TailScratch {
+  void* fixed = nullptr;    // non-null: this region of fixed_bytes, no allocation
+  size_t fixed_bytes = 0;
+};
+
 // One launch with tiles `tn` columns wide (kTN, or kTNNarrow on the TMA
 // path only: returns kRetryWide, having launched nothing, when TMA cannot be
-// used after all).
+// used after all).  With a fixed scratch region, a split tail that needs
+// more than it holds returns GEMM_F32_ESCRATCH, having launched nothing.
 constexpr int kRetryWide = 1;
 
-int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launches) {
+int launch_tc_tn(GemmArgs& g, int nprod, int tn, const TailScratch& scratch, cudaStream_t stream,
+                 int* launches) {
   *launches = 0;
   int bk = 0;
   TcParams p;
@@ -905,8 +915,14 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
       ws_bytes = plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * tn * sizeof(float));
   }
   void* ws = nullptr;
-  int must_clear = 0;
-  if (ws_bytes) ws = acquire_workspace(g.device, stream, ws_bytes, &must_clear);
+  if (ws_bytes) {
+    if (scratch.fixed) {
+      if (ws_bytes > scratch.fixed_bytes) return GEMM_F32_ESCRATCH;
+      ws = scratch.fixed;
+    } else {
+      ws = acquire_workspace(g.device, stream, ws_bytes);
+    }
+  }
   if (!ws) {
     tm = one_wave_tm ? one_wave_tm : choose_tm(g, false, tn);
     bk = bk_for(nprod, tm, tma_ok);
@@ -921,15 +937,8 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
   int grid;
   if (ws) {
     grid = g.num_sms;
-    p.counters = static_cast<unsigned*>(ws);
+    p.counters = static_cast<unsigned long long*>(ws);
     p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
-    if (must_clear) {
-      if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return GEMM_F32_ELAUNCH;
-      }
-      *launches += 1;
-    }
   } else {
     p.dp_tiles = static_cast<int>(tiles);
     grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
@@ -967,6 +976,19 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, cudaStream_t stream, int* launc
   return rc;
 }
 
+// The single-CTA kernel for a problem: tiles 64 columns wide for N <= 64 on
+// the TMA path, so that no MMA work is spent on columns beyond N (measured on
+// GB300: 65536 x 1024 x 64 had the tensor pipe 79 % busy with half of each
+// M = 128 MMA discarded), 128 columns otherwise.
+int launch_tc_single(GemmArgs& g, int nprod, const TailScratch& scratch, cudaStream_t stream,
+                     int* launches) {
+  if (g.N <= kTNNarrow && !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && tma_addressable(g)) {
+    const int rc = launch_tc_tn(g, nprod, kTNNarrow, scratch, stream, launches);
+    if (rc != kRetryWide) return rc;
+  }
+  return launch_tc_tn(g, nprod, kTN, scratch, stream, launches);
+}
+
 int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 
 int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
@@ -995,14 +1017,7 @@ int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches
   if (nprod == 1 && !(g.flags & no_pair) && tma_addressable(g) && g.M >= 256 && g.N >= 256 &&
       !one_wave_height(g, kTN))
     return launch_tc_pair(g, nprod, stream, launches);
-  // N <= 64: tiles 64 columns wide and an M = 64 MMA, so that no MMA work is
-  // spent on columns beyond N (measured on GB300: 65536 x 1024 x 64 had the
-  // tensor pipe 79 % busy with half of each M = 128 MMA discarded)
-  if (g.N <= kTNNarrow && !(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && tma_addressable(g)) {
-    const int rc = launch_tc_tn(g, nprod, kTNNarrow, stream, launches);
-    if (rc != kRetryWide) return rc;
-  }
-  return launch_tc_tn(g, nprod, kTN, stream, launches);
+  return launch_tc_single(g, nprod, TailScratch(), stream, launches);
 }
 
 // ---------------------------------------------------------------- fixed-scratch variant
@@ -1010,101 +1025,31 @@ int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches
 // gemm_f32_noalloc, compiled into the library instead of allocated: every
 // device that loads this module holds these bytes until the process exits.
 // All calls on a device share it, so calls that overlap on the GPU race.
+// Being zero at load, its tile counters start in a valid state; afterwards
+// they keep themselves valid (generation scheme, device_common.cuh).
 static __device__ __align__(256) unsigned char g_fixed_scratch[GEMM_F32_NOALLOC_SCRATCH_BYTES];
 
-namespace {
+void* fixed_scratch_address() {
+  // In host code g_fixed_scratch only names the array: its device address on
+  // the current device is asked of the runtime.  Under lazy module loading
+  // this loads this file's module (and so places the array) if it was not
+  // loaded yet.
+  void* ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_fixed_scratch) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return ptr;
+}
 
-struct FixedScratch {
-  std::once_flag once;
-  void* ptr = nullptr;   // device address of g_fixed_scratch on this device
-};
-FixedScratch g_fixed[kMaxDevices];
-
-}  // namespace
-
-int launch_tc_fixed_scratch(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
+int launch_tc_fixed_scratch(GemmArgs& g, int nprod, void* scratch, cudaStream_t stream,
+                            int* launches) {
   *launches = 0;
-  if (g.device < 0 || g.device >= kMaxDevices) return GEMM_F32_EDEVICE;
-  // In host code g_fixed_scratch only names the array; its device address is
-  // asked for once per device, with that device current (the caller's).
-  FixedScratch& fs = g_fixed[g.device];
-  std::call_once(fs.once, [&fs] {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_fixed_scratch) == cudaSuccess)
-      fs.ptr = ptr;
-    else
-      (void)cudaGetLastError();
-  });
-  if (!fs.ptr) return GEMM_F32_EDEVICE;
-
-  TcParams p;
-  p.A = g.A;
-  p.B = g.B;
-  p.C = g.C;
-  p.M = g.M;
-  p.N = g.N;
-  p.K = g.K;
-  p.tiles_n = ceil_div(g.N, kTN);
-  p.drop_first_copy = 0;
-  p.err = g.err;
-  const TcGeneral gp = general_of(g);
-  p.partials = nullptr;
-  p.counters = nullptr;
-  const bool tma_ok = tma_addressable(g);
-  int tm = choose_tm(g, true, kTN);
-  int bk = bk_for(nprod, tm, tma_ok);
-  p.k_iters = ceil_div(g.K, bk);
-  p.tiles_m = ceil_div(g.M, tm);
-  long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
-  if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
-  const size_t need =
-      plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * kTN * sizeof(float));
-  if (need > GEMM_F32_NOALLOC_SCRATCH_BYTES) return GEMM_F32_ESCRATCH;
-  int grid;
-  if (need) {
-    grid = g.num_sms;
-    p.counters = static_cast<unsigned*>(fs.ptr);
-    p.partials = reinterpret_cast<float*>(static_cast<char*>(fs.ptr) + kCounterBytes);
-    // the counters must start at zero; the array holds whatever the last
-    // call (or a call that gave up on a wait) left there
-    if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return GEMM_F32_ELAUNCH;
-    }
-    *launches += 1;
-  } else {
-    tm = choose_tm(g, false, kTN);
-    bk = bk_for(nprod, tm, tma_ok);
-    p.k_iters = ceil_div(g.K, bk);
-    p.tiles_m = ceil_div(g.M, tm);
-    tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
-    if (tiles > 0x7fffffffL) return GEMM_F32_EINVAL;
-    p.dp_tiles = static_cast<int>(tiles);
-    p.sk_ctas = 0;
-    p.sk_work = 0;
-    p.max_seg = 1;
-    grid = static_cast<int>(std::min<long>(tiles, g.num_sms));
-  }
-
-  bool tma = tma_addressable(g);
-  alignas(64) CUtensorMap ma, mb;
-  if (tma) {
-    tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, tm,
-                    bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, g.ldb, kTN, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
-  }
-  if (!tma) {
-    memset(&ma, 0, sizeof(ma));
-    memset(&mb, 0, sizeof(mb));
-  }
-  const int rc = nprod == 3
-                     ? launch_loader<3>(tma, tm, bk, g, p, gp, ma, mb, grid, stream)
-                     : launch_loader<1>(tma, tm, bk, g, p, gp, ma, mb, grid, stream);
-  if (rc == GEMM_F32_OK) {
-    *launches += 1;
-    g.kernel = "tc_gemm_kernel";
-  }
-  return rc;
+  if (!scratch) return GEMM_F32_EDEVICE;
+  TailScratch fixed;
+  fixed.fixed = scratch;
+  fixed.fixed_bytes = GEMM_F32_NOALLOC_SCRATCH_BYTES;
+  return launch_tc_single(g, nprod, fixed, stream, launches);
 }
 
 }  // namespace gemm_f32_impl

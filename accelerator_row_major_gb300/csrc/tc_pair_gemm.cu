@@ -70,7 +70,7 @@ struct PairParams {
   long long sk_work;
   int max_seg;
   float* partials;                   // [tail][max_seg][2][256 m][128 n]
-  unsigned* counters;                // [tail][2]
+  unsigned long long* counters;      // [tail][2]: generation and partials published
   int drop_first_copy;
   unsigned* err;
 };
@@ -503,7 +503,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __threadfence();
         epilogue_sync();
         if (nl == 0 &&
-            atomicAdd(p.counters + 2 * w.tail + rank, 1u) == static_cast<unsigned>(w.nseg - 1)) {
+            tail_arrive(p.counters, 2 * w.tail + static_cast<int>(rank)) ==
+                static_cast<unsigned>(w.nseg)) {
           if (*pending_count < kMaxPending)
             pending[(*pending_count)++] = w;
           else
@@ -705,9 +706,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (threadIdx.x == 0) p.counters[2 * pw.tail + rank] = 0;
     }
   }
+  if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
 }
 
 // ---------------------------------------------------------------- host side
@@ -824,21 +825,13 @@ int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   if (!(g.flags & GEMM_F32_FLAG_NO_SPLIT_K)) {
     PairParams q = p;
     const size_t ws_bytes =
-        plan_split_tail(q, tiles, pairs, sizeof(float) * 2 * kPairTile * kHalf);
-    int must_clear = 0;
-    void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes, &must_clear) : nullptr;
+        plan_split_tail(q, tiles, pairs, sizeof(float) * 2 * kPairTile * kHalf, kMinSplitIters, 2);
+    void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes) : nullptr;
     if (ws) {
       p = q;
       units = pairs;
-      p.counters = static_cast<unsigned*>(ws);
+      p.counters = static_cast<unsigned long long*>(ws);
       p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
-      if (must_clear) {
-        if (cudaMemsetAsync(p.counters, 0, kCounterBytes, stream) != cudaSuccess) {
-          (void)cudaGetLastError();
-          return GEMM_F32_ELAUNCH;
-        }
-        *launches += 1;
-      }
     }
   }
   const int grid = 2 * units;

@@ -54,7 +54,10 @@ enum gemm_f32_status_code {
     GEMM_F32_ELAUNCH = -3,  /* the kernel launch (or the K == 0 memset) was
                                refused by the CUDA runtime                  */
     GEMM_F32_ETIMEOUT = -4, /* gemm_f32_status(): a bounded device-side wait
-                               ran out; C of that call is undefined         */
+                               ran out; C of that call is undefined.  Later
+                               calls are not affected: the split-tail
+                               bookkeeping the call left half done is
+                               ignored by the next call on its own          */
     GEMM_F32_ESCRATCH = -5  /* gemm_f32_noalloc(): the product would need
                                more scratch than the library's fixed array
                                (GEMM_F32_NOALLOC_SCRATCH_BYTES); nothing was
@@ -135,9 +138,8 @@ int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K,
 int gemm_f32_status(gemm_f32_stream_t stream, unsigned* site);
 
 /* Number of kernels the last successful call on this host thread launched
- * (0 for a no-op, 1 for a GEMM or for the K == 0 memset, plus one when a
- * split-tail workspace had to be re-zeroed first and one per operand copied
- * for the tensor-memory accelerator). */
+ * (0 for a no-op, 1 for a GEMM or for the K == 0 memset, plus one per launch
+ * that copied operands for the tensor-memory accelerator). */
 int gemm_f32_last_launches(void);
 
 /* Name of the kernel the last successful call on this host thread launched:
@@ -194,20 +196,32 @@ int gemm_f32_release(void);
  * device memory to its own pool, a latency-critical path that cannot take
  * cudaMalloc's implicit device synchronisation, or an embedding that must
  * keep the library's memory footprint fixed after start-up.  gemm_f32_ex may
- * allocate its split-tail workspace on first use; this call takes that
- * scratch from a fixed array inside the library instead and never calls
- * cudaMalloc, cudaFree or any allocating routine.
+ * allocate its split-tail workspace or aligned copies of its operands on
+ * first use; this call takes the split tail's scratch from a fixed array
+ * inside the library instead and never calls cudaMalloc, cudaFree or any
+ * allocating routine.
  *   - The caller still passes A, B and C (device pointers, as gemm_f32).
- *   - The first call on a device looks up the array's device address (a
- *     one-time set-up); make that first call before any stream capture.
+ *   - The array's device address is looked up when the library first sets
+ *     up a device (the first call of any entry point there), which loads
+ *     the library's module holding the array.  Make one library call on each
+ *     device before the caller's pool takes the device memory and before
+ *     any stream capture; if that lookup failed, this call retries it.
  *   - Every call on a device shares the one array, which keeps what the
  *     last call left in it: two such calls whose kernels overlap on the GPU
- *     (for example on two streams) race and give wrong results.  Each call
- *     re-zeroes the part of the array that must start at zero.
+ *     (for example on two streams) race and give wrong results.  The array's
+ *     split-tail counters need no clearing between calls: they carry a
+ *     generation that each call moves on.
+ *   - It always runs the single-CTA tensor kernel (tiles 128 columns wide,
+ *     or 64 for N <= 64 with TMA-readable operands), never the CTA-pair
+ *     kernel nor operand copies, so on large squares (the pair kernel's
+ *     domain) and on operands TMA cannot read (per-thread loads) it is
+ *     slower than gemm_f32_ex, and its summation order can differ: the
+ *     result meets the same bound as gemm_f32_ex in that mode, but need not
+ *     be bitwise equal to it.
  *   - Returns GEMM_F32_ESCRATCH, launching nothing, when the product's
  *     split tail would need more than GEMM_F32_NOALLOC_SCRATCH_BYTES; other
- *     errors as gemm_f32_ex (GEMM_F32_EINVAL for mode FFMA or a bad mode).
- * The result equals gemm_f32_ex's for the same mode. */
+ *     errors as gemm_f32_ex (GEMM_F32_EINVAL for mode FFMA or a bad mode,
+ *     GEMM_F32_EDEVICE if the array's address cannot be had). */
 int gemm_f32_noalloc(const float* A, const float* B, float* C, int M, int N, int K,
                      int mode, gemm_f32_stream_t stream);
 
@@ -257,6 +271,36 @@ int gemm_f32_general(int trans_a, int trans_b, int M, int N, int K, float alpha,
  * and 2, M > 4194240 for steps 3 and 4).  Allocates nothing. */
 int gemm_f32_ladder(const float* A, const float* B, float* C, int M, int N, int K, int step,
                     gemm_f32_stream_t stream);
+
+/* Per-SM arithmetic rates of the units the kernels run on, measured on the
+ * current device: the compute peaks of the roofline ("Lesson 10:
+ * shared-memory tiled GEMM", hpc.payai.win, section 1, which judges a
+ * kernel against the peak of the unit doing its work).  Each figure is
+ * FLOP per SM per SM clock cycle (2 per multiply-add), the median over the
+ * SMs of kernels that do nothing else -- no loads, no stores in the timed
+ * span -- counted with the SM's own cycle counter, so it holds at any clock:
+ *   tf32_flop_per_clk_sm       tcgen05.mma kind::tf32, cta_group::1,
+ *                              M = 128, N = 256, K = 8, back to back
+ *   tf32_pair_flop_per_clk_sm  the same on SM pairs (cta_group::2, M = 256),
+ *                              per SM
+ *   ffma_flop_per_clk_sm       fma.rn.f32x2 chains, 16 warps per SM
+ *   sm_mhz                     SM clock during the probes (cycles over
+ *                              globaltimer nanoseconds), median
+ *   num_sms                    multiprocessors of the device
+ * A peak in FLOP/s is rate x num_sms x the clock the measured kernel ran at.
+ * Synchronises the device, allocates and frees a small buffer, takes a few
+ * milliseconds.  Returns 0, GEMM_F32_EINVAL (null pointer), GEMM_F32_EDEVICE
+ * (not sm_103), GEMM_F32_ELAUNCH or GEMM_F32_ETIMEOUT (the bounded wait for
+ * the MMAs ran out). */
+typedef struct {
+    double tf32_flop_per_clk_sm;
+    double tf32_pair_flop_per_clk_sm;
+    double ffma_flop_per_clk_sm;
+    double sm_mhz;
+    int num_sms;
+} gemm_f32_unit_rates_t;
+
+int gemm_f32_unit_rates(gemm_f32_unit_rates_t* rates);
 
 /* Static version string, e.g. "gemm_f32 1.0 sm_103a". */
 const char* gemm_f32_version(void);

@@ -50,8 +50,8 @@ def run_abi(A: np.ndarray, B: np.ndarray, mode="tc3x", flags=0, offset_a=0, offs
         else:
             rc = g.gemm_f32_ladder(a_ptr, b_ptr, c_ptr, M, N, K, ladder_step, s)
         assert rc == g.GEMM_F32_OK, "the call returned %d" % rc
-        # the product, plus a counter reset and up to two operand copies
-        expect = (0,) if (M == 0 or N == 0) else (1, 2, 3, 4)
+        # the product, plus up to two launches copying operands for TMA
+        expect = (0,) if (M == 0 or N == 0) else (1, 2, 3)
         assert g.gemm_f32_last_launches() in expect
         st, site = g.gemm_f32_status(s)
         assert st == g.GEMM_F32_OK, "device error word: site %d" % site
@@ -74,6 +74,11 @@ def assert_close(C: np.ndarray, Co: np.ndarray, absAB: np.ndarray, tol: float, w
         raise AssertionError("%s: %d elements out of bound; first (%d,%d): got %r want %r absAB %r; "
                              "max err/absAB %.3e" % (what, bad.sum(), i, j, C[i, j], Co[i, j],
                                                      absAB[i, j], ratio))
+
+
+# (what, max err / (|A||B|), bound) of the full-size comparisons, printed in
+# the terminal summary (tests/conftest.py)
+ERROR_REPORT = []
 
 
 def max_rel_err(C, Co, absAB):

@@ -28,3 +28,15 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """The largest error relative to (|A||B|)_ij of every full-size parity
+    comparison that ran, per problem and mode."""
+    rows = sys.modules.get("tests._gpu")
+    rows = getattr(rows, "ERROR_REPORT", None) if rows else None
+    if not rows:
+        return
+    terminalreporter.section("max |C - C_oracle| / (|A||B|)_ij over every element")
+    for what, ratio, tol in rows:
+        terminalreporter.write_line("%-34s %.3e  (bound %.0e)" % (what, ratio, tol))

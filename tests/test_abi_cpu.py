@@ -24,7 +24,7 @@ def test_header_declares_the_entry_points(g):
     assert names == sorted(["gemm_f32", "gemm_f32_ex", "gemm_f32_status", "gemm_f32_ladder",
                             "gemm_f32_general", "gemm_f32_host",
                             "gemm_f32_last_kernel", "gemm_f32_last_launches", "gemm_f32_noalloc",
-                            "gemm_f32_release",
+                            "gemm_f32_release", "gemm_f32_unit_rates",
                             "gemm_f32_version"])
 
 

@@ -48,3 +48,37 @@ def test_ffma_ignores_the_test_flag():
     Co, absAB = oracle_full(A, B)
     C, _ = run_abi(A, B, "ffma", g.FLAG_TEST_DROP_COPY)
     assert_close(C, Co, absAB, TOL["ffma"], "ffma with test flag")
+
+
+@pytest.mark.parametrize("mode,flags", [("tc3x", 0), ("tc3x", 0x800), ("tc1x", 0)])
+def test_split_tail_after_a_timeout_needs_no_status_call(mode, flags):
+    """A split-tail call whose bounded waits run out leaves some tile
+    counters of its workspace half counted (CTA 0 never publishes its
+    partials).  The next split-tail call on the same stream, made without
+    gemm_f32_status() in between, must still pick the right CTA to sum each
+    tile: its whole C is compared with the oracle.  3000 x 4096 x 2000
+    splits its last wave along K on the CTA-pair kernel (default) and on the
+    single-CTA kernel (0x800)."""
+    import torch
+
+    g = lib()
+    M, K, N = 3000, 4096, 2000
+    A, B = workloads.make_inputs(M, K, N, "normal", 41)
+    Co, absAB = oracle_full(A, B)
+    dev = torch.device("cuda:0")
+    At = torch.from_numpy(A).to(dev)
+    Bt = torch.from_numpy(B).to(dev)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    s = torch.cuda.current_stream(dev)
+    assert g.gemm_f32_ex(At, Bt, C, M, N, K, mode, flags, s) == g.GEMM_F32_OK
+    assert g.gemm_f32_status(s) == (g.GEMM_F32_OK, 0)
+    assert g.gemm_f32_ex(At, Bt, C, M, N, K, mode, flags | g.FLAG_TEST_DROP_COPY, s) == g.GEMM_F32_OK
+    for call in range(2):
+        C.fill_(float("nan"))
+        assert g.gemm_f32_ex(At, Bt, C, M, N, K, mode, flags, s) == g.GEMM_F32_OK
+        st, site = g.gemm_f32_status(s)
+        if call == 0:
+            assert st == g.GEMM_F32_ETIMEOUT and site in range(1, 9)
+        else:
+            assert (st, site) == (g.GEMM_F32_OK, 0)
+        assert_close(C.cpu().numpy(), Co, absAB, TOL[mode], "call %d after a timeout/%s/%#x" % (call, mode, flags))
