@@ -2,7 +2,9 @@
 
 Every computation happens in the library's CUDA kernels.  The library is
 loaded on first use; if it is missing, that first call raises ImportError.
-There is no fallback.
+There is no fallback.  The environment variable GEMM_F32_LIBRARY, when set,
+names the library file to load instead (the tests use it to run on the
+bounds-checked debug build, libgemm_f32_checked.so).
 """
 from __future__ import annotations
 
@@ -11,7 +13,7 @@ import os
 import re
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libgemm_f32.so")
+LIB_PATH = os.environ.get("GEMM_F32_LIBRARY") or os.path.join(_PKG, "libgemm_f32.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "gemm_f32.h")
 
 GEMM_F32_OK = 0
@@ -30,6 +32,7 @@ MODES = {"tc3x": MODE_TC3X, "ffma": MODE_FFMA, "tc1x": MODE_TC1X}
 FLAG_FORCE_STAGED = 0x1
 FLAG_TILE64 = 0x10
 FLAG_TILE128 = 0x20
+FLAG_TILE224 = 0x80
 FLAG_TILE256 = 0x40
 FLAG_ONE_TILE_PER_CTA = 0x100
 FLAG_NO_SPLIT_K = 0x200
@@ -63,7 +66,7 @@ class UnitRates(ctypes.Structure):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError("libgemm_f32.so is not built (run accelerator_row_major_gb300.build.build())")
+        raise ImportError("%s is not built (run accelerator_row_major_gb300.build.build())" % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
     vp, ci, cu = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint
     lib.gemm_f32.argtypes = [vp, vp, vp, ci, ci, ci, vp]

@@ -1,6 +1,11 @@
 """Builds libgemm_f32.so in-tree with nvcc for sm_103a (no GPU needed).
 
-    python -m accelerator_row_major_gb300.build [--verbose-ptxas]
+    python -m accelerator_row_major_gb300.build [--verbose-ptxas] [--checked]
+
+--checked builds the debug library libgemm_f32_checked.so instead: the same
+sources with -DGEMM_BOUNDS_CHECK, in which every hand-indexed global load
+and store is checked against its array's extent and a violation is reported
+through gemm_f32_status() (site codes 16-20) instead of being made.
 
 Each .cu under csrc/ is compiled to an object in parallel, then linked into
 a shared library with the CUDA runtime linked statically, so loading the
@@ -20,6 +25,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libgemm_f32.so")
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libgemm_f32_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
               "--expt-relaxed-constexpr", "-Xptxas", "-warn-spills"]
@@ -41,16 +48,17 @@ def _deps():
         [os.path.join(os.path.dirname(PKG), "include", "gemm_f32.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+def _compile(src: str, verbose_ptxas: bool, checked: bool = False) -> str:
+    obj = os.path.join(BUILD_CHECKED if checked else BUILD, os.path.basename(src) + ".o")
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *(["-DGEMM_BOUNDS_CHECK"] if checked else []), "-c", src,
+           "-o", obj]
     if verbose_ptxas:
         cmd += ["-Xptxas", "-v"]
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -61,21 +69,22 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not verbose_ptxas and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = False) -> str:
+    lib = LIB_CHECKED if checked else LIB
+    if not force and not verbose_ptxas and up_to_date(lib):
+        return lib
+    os.makedirs(BUILD_CHECKED if checked else BUILD, exist_ok=True)
     srcs = _sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), srcs))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas, checked), srcs))
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force=True, verbose_ptxas="--verbose-ptxas" in sys.argv))
+    print(build(force=True, verbose_ptxas="--verbose-ptxas" in sys.argv, checked="--checked" in sys.argv))

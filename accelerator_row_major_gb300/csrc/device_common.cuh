@@ -37,6 +37,45 @@ __device__ __forceinline__ void record_error(unsigned* err, unsigned site) {
   atomicCAS(err, 0u, site);
 }
 
+// ---------------------------------------------------------------- bounds checks
+// The debug build (-DGEMM_BOUNDS_CHECK, libgemm_f32_checked.so) checks every
+// global load and store that a kernel indexes by hand -- the per-thread
+// operand loads, the FFMA copies, the C stores, the partial tiles of the
+// split tail, the operand packing and the teaching kernels -- against the
+// extent of the array it addresses.  An index outside records its site in
+// the error word (the first one wins, as for the waits), and the access is
+// skipped: a load gives 0, a store does not happen.  Out-of-range elements
+// load 0 and are never written, the rule of "Lesson 10: shared-memory tiled
+// GEMM" (hpc.payai.win, section 3); here it is checked, not assumed.  In the
+// default build the check is the constant true and costs nothing.
+enum BoundsSite : unsigned {
+  kSiteBoundsA = 16,        // a read of A outside its stored extent
+  kSiteBoundsB = 17,        // a read of B outside its stored extent
+  kSiteBoundsC = 18,        // a read or write of C outside its window's extent
+  kSiteBoundsWork = 19,     // a partial tile outside the split-tail workspace
+  kSiteBoundsPack = 20,     // operand packing outside its source or destination
+};
+
+#ifdef GEMM_BOUNDS_CHECK
+__device__ __forceinline__ bool in_extent(size_t index, size_t extent, unsigned* err,
+                                          unsigned site) {
+  if (index < extent) return true;
+  record_error(err, site);
+  return false;
+}
+#define GEMM_IN_EXTENT(index, extent, err, site) \
+  ::gemm_f32_dev::in_extent(static_cast<size_t>(index), static_cast<size_t>(extent), (err), (site))
+#else
+#define GEMM_IN_EXTENT(index, extent, err, site) true
+#endif
+
+// Elements spanned by a row-major array of `rows` rows of `cols` elements
+// with row stride `ld` (first to last element touched).
+__host__ __device__ __forceinline__ size_t stored_extent(long long rows, long long cols,
+                                                         long long ld) {
+  return rows > 0 && cols > 0 ? static_cast<size_t>((rows - 1) * ld + cols) : 0;
+}
+
 // ---------------------------------------------------------------- tile order
 // Output tiles are visited in groups of `group` tile-rows: inside a group the
 // index runs down the rows first, so CTAs that run at the same time share
@@ -223,9 +262,18 @@ inline size_t plan_split_tail(P& p, long tiles, int grid, size_t partial_tile_by
 // thread per partial keep the L2 reads in flight; a kernel whose hot loops
 // need few registers takes a small CHUNK so that this end-of-work code does
 // not set its register count.
+// What the checked build checks the reduction's accesses against: the error
+// word, the elements of partials from `parts` on, and C's extent.
+struct BoundsRef {
+  unsigned* err;
+  size_t parts_extent;
+  size_t c_extent;
+};
+
 template <int ROWS, int COLS, int NTHREADS, int CHUNK>
 __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, int m0, int n0,
-                                                int M, int N, float* C) {
+                                                int M, int N, float* C,
+                                                [[maybe_unused]] const BoundsRef& br) {
   constexpr int kVec = ROWS * COLS / 4;            // float4s per partial
   constexpr int kPer = kVec / NTHREADS;            // per thread
   constexpr int kChunk = kPer < CHUNK ? kPer : CHUNK;
@@ -240,8 +288,12 @@ __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, in
     for (int sg = 0; sg < nseg; ++sg) {
       float4 x[kChunk];
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i)
-        x[i] = __ldcg(p4 + static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS);
+      for (int i = 0; i < kChunk; ++i) {
+        const size_t f4 = static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS;
+        x[i] = GEMM_IN_EXTENT(4 * f4 + 3, br.parts_extent, br.err, kSiteBoundsWork)
+                   ? __ldcg(p4 + f4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
         sum[i].x += x[i].x;
@@ -260,7 +312,8 @@ __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, in
         const float v[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          if (n + q < N) dst[q] = v[q];
+          if (n + q < N && GEMM_IN_EXTENT(dst + q - C, br.c_extent, br.err, kSiteBoundsC))
+            dst[q] = v[q];
       }
     }
   }
@@ -271,7 +324,8 @@ __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, in
 template <int ROWS, int COLS, int NTHREADS, int CHUNK>
 __device__ __forceinline__ void reduce_partials_general(const float* parts, int nseg, int m0,
                                                         int n0, int M, int N, float* C, int ldc,
-                                                        int scale, float alpha, float beta) {
+                                                        int scale, float alpha, float beta,
+                                                        [[maybe_unused]] const BoundsRef& br) {
   constexpr int kVec = ROWS * COLS / 4;            // float4s per partial
   constexpr int kPer = kVec / NTHREADS;            // per thread
   constexpr int kChunk = kPer < CHUNK ? kPer : CHUNK;
@@ -286,8 +340,12 @@ __device__ __forceinline__ void reduce_partials_general(const float* parts, int 
     for (int sg = 0; sg < nseg; ++sg) {
       float4 x[kChunk];
 #pragma unroll
-      for (int i = 0; i < kChunk; ++i)
-        x[i] = __ldcg(p4 + static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS);
+      for (int i = 0; i < kChunk; ++i) {
+        const size_t f4 = static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS;
+        x[i] = GEMM_IN_EXTENT(4 * f4 + 3, br.parts_extent, br.err, kSiteBoundsWork)
+                   ? __ldcg(p4 + f4)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
 #pragma unroll
       for (int i = 0; i < kChunk; ++i) {
         sum[i].x += x[i].x;
@@ -306,7 +364,8 @@ __device__ __forceinline__ void reduce_partials_general(const float* parts, int 
         const float v[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          if (n + q >= N) continue;
+          if (n + q >= N || !GEMM_IN_EXTENT(dst + q - C, br.c_extent, br.err, kSiteBoundsC))
+            continue;
           float r = v[q];
           if (scale) {   // alpha * sum (+ beta * C_old when beta != 0)
             r *= alpha;
@@ -407,6 +466,31 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* desc, uint
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(desc), "r"(bar), "r"(x), "r"(y)
       : "memory");
+}
+
+// The same with an L2 eviction-priority policy for the copied lines (from
+// l2_policy_evict_first / l2_policy_evict_last).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* desc, uint32_t bar, int x,
+                                                 int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(desc), "r"(bar), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
+// L2 policies: lines read once soon (evicted before others) and lines read
+// again later (evicted after others).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // ---------------------------------------------------------------- tcgen05

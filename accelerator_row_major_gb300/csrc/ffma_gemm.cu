@@ -1,7 +1,10 @@
-// CUDA-core FP32 GEMM (FFMA) for sm_103a: persistent CTAs, 128 x 256 output
-// tiles, 8 x 16 outputs per thread, a 4-stage cp.async shared-memory ring,
-// and the paired fp32 fused multiply-add (fma.rn.f32x2: two FMAs per lane
-// per instruction, each rounded once like fmaf).
+// CUDA-core FP32 GEMM (FFMA) for sm_103a: persistent CTAs, 8 x 16 outputs
+// per thread, a 4-stage cp.async shared-memory ring, and the paired fp32
+// fused multiply-add (fma.rn.f32x2: two FMAs per lane per instruction, each
+// rounded once like fmaf).  Block tiles: 128 x 256 (256 threads, one CTA per
+// SM); 256 x 64 for N <= 64 and 64 x 256 for M <= 64 (128 threads, two CTAs
+// per SM), so that skinny products spend no multiply-adds on rows or
+// columns beyond the matrix.
 //
 // Computes C[i][j] = sum_k A[i][k] * B[k][j] (row-major) in fp32 fused
 // multiply-adds, k ascending per output.  The structure follows the pages'
@@ -19,10 +22,14 @@
 // The last partial wave is split along K like the tensor-core path's (see
 // device_common.cuh): partial tiles go through the library's workspace.
 //
-// Thread (tx, ty) of the 16 x 16 grid owns rows ty + 16 i (i < 8) and
-// columns 64 g + 4 tx .. +3 (g < 4).  A warp covers 4 values of ty and 8 of
-// tx, so per K step its 16-byte A reads hit 4 consecutive rows (distinct
-// banks with the 20-float row pitch) and its B reads one 128-byte segment.
+// Thread (tx, ty) of the TX x TY grid (TX = BN / 16, TY = BM / 8) owns rows
+// ty + TY i (i < 8) and columns (BN / 4) g + 4 tx .. +3 (g < 4).  A warp
+// covers min(TX, 8) values of tx and the rest of its lanes along ty, so per
+// K step its 16-byte A reads hit 4 or 8 consecutive rows (distinct banks
+// with the 20-float row pitch) and its B reads one 128- or 64-byte segment.
+// The block tile is a template parameter: the pages' last step makes the
+// block and thread tiles (BM, BN, TM, TN) parameters of the kernel for the
+// same reason ("LeetGPU problem 2", section v4).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -38,14 +45,29 @@ using namespace gemm_f32_dev;
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 16;
+constexpr int kBK = 16;
 constexpr int kStages = 4;
-constexpr int kThreads = 256;
 constexpr int kAPitch = kBK + 4;               // floats per A row in shared memory
-constexpr int kAStage = kBM * kAPitch;         // floats
-constexpr int kBStage = kBK * kBN;             // floats
-constexpr int kSmemBytes = kStages * (kAStage + kBStage) * 4;
 constexpr int kRasterGroup = 8;
+
+// A block tile of BM x BN outputs, 8 x 16 per thread.
+template <int BM_, int BN_>
+struct FfmaTile {
+  static constexpr int BM = BM_, BN = BN_;
+  static constexpr int TY = BM / 8, TX = BN / 16;       // threads along rows / columns
+  static constexpr int THREADS = TX * TY;
+  static constexpr int LX = TX < 8 ? TX : 8;              // lanes of a warp along columns
+  static constexpr int WX = TX / LX;                      // warps along columns
+  static constexpr int CG = BN / 4;                       // column-group stride
+  static constexpr int CTAS_PER_SM = 256 / THREADS;       // 8 warps per SM
+  static constexpr int A_STAGE = BM * kAPitch;            // floats
+  static constexpr int B_STAGE = kBK * BN;                // floats
+  static constexpr int SMEM = kStages * (A_STAGE + B_STAGE) * 4;
+  static_assert(THREADS % 32 == 0 && BM * 4 % THREADS == 0 && BN * 4 % THREADS == 0, "tile");
+};
+using TileWide = FfmaTile<128, 256>;     // default
+using TileTall = FfmaTile<256, 64>;      // N <= 64
+using TileShort = FfmaTile<64, 256>;     // M <= 64
 constexpr int kMaxPending = 8;               // split tiles one CTA may have to reduce
 // An FFMA K iteration costs ~6x a tensor-core one, so splitting the tail pays
 // off at far fewer iterations per CTA (measured on GB300: 2.5x on 1024 x 512 x
@@ -62,7 +84,7 @@ struct FfmaParams {
   int sk_ctas;           // CTAs 0 .. sk_ctas-1 share the K iterations of the rest
   long long sk_work;     // (tiles - dp_tiles) * k_iters
   int max_seg;           // most CTAs sharing one tail tile
-  float* partials;       // [tail tile][max_seg][128][256] fp32
+  float* partials;       // [tail tile][max_seg][BM][BN] fp32
   unsigned long long* counters;   // [tail tile]: generation and partials published
   unsigned* err;
 };
@@ -123,7 +145,7 @@ __device__ __forceinline__ void cp_async_wait() {
 // multiple of 4 and 16-byte aligned A and B, so a 16-byte chunk is either
 // wholly inside the matrix or wholly outside.  Otherwise 4-byte copies, which
 // also read transposed storage.
-template <bool VEC, bool GEN>
+template <class T, bool VEC, bool GEN>
 __device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGeneral& gp, int m0,
                                            int n0, int kt,
                                            uint32_t a_dst, uint32_t b_dst) {
@@ -131,44 +153,54 @@ __device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGenera
   const int k0 = kt * kBK;
   const int lda = GEN ? gp.lda : p.K, ldb = GEN ? gp.ldb : p.N;
   const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
-  // A: 128 rows x 16 k = 512 chunks of 4 floats; thread -> chunks tid, tid + 256
+  [[maybe_unused]] const size_t a_extent =
+      trans_a ? stored_extent(p.K, p.M, lda) : stored_extent(p.M, p.K, lda);
+  [[maybe_unused]] const size_t b_extent =
+      trans_b ? stored_extent(p.N, p.K, ldb) : stored_extent(p.K, p.N, ldb);
+  // A: BM rows x 16 k = 4 BM chunks of 4 floats; thread -> chunks tid + THREADS h
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int c = tid + h * kThreads;
+  for (int h = 0; h < T::BM * 4 / T::THREADS; ++h) {
+    const int c = tid + h * T::THREADS;
     const int r = c >> 2, kc = (c & 3) * 4;
     const int gm = m0 + r, gk = k0 + kc;
     const uint32_t dst = a_dst + (r * kAPitch + kc) * 4;
     if (VEC) {
-      const bool in = gm < p.M && gk < p.K;
+      const bool in = gm < p.M && gk < p.K &&
+                      GEMM_IN_EXTENT(static_cast<size_t>(gm) * lda + gk + 3, a_extent, p.err,
+                                     kSiteBoundsA);
       const float* src = in ? p.A + static_cast<size_t>(gm) * lda + gk : p.A;
       cp_async_16(dst, src, in ? 16u : 0u);
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool in = gm < p.M && gk + e < p.K;
         const size_t at = trans_a ? static_cast<size_t>(gk + e) * lda + gm
                                   : static_cast<size_t>(gm) * lda + gk + e;
+        const bool in = gm < p.M && gk + e < p.K &&
+                        GEMM_IN_EXTENT(at, a_extent, p.err, kSiteBoundsA);
         cp_async_4(dst + 4 * e, in ? p.A + at : p.A, in ? 4u : 0u);
       }
     }
   }
-  // B: 16 k x 256 columns = 1024 chunks; thread -> chunks tid + 256 h
+  // B: 16 k x BN columns = 4 BN chunks; thread -> chunks tid + THREADS h
 #pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    const int c = tid + h * kThreads;
-    const int k = c >> 6, nc = (c & 63) * 4;
+  for (int h = 0; h < T::BN * 4 / T::THREADS; ++h) {
+    const int c = tid + h * T::THREADS;
+    const int k = c / (T::BN / 4), nc = (c % (T::BN / 4)) * 4;
     const int gk = k0 + k, gn = n0 + nc;
-    const uint32_t dst = b_dst + (k * kBN + nc) * 4;
+    const uint32_t dst = b_dst + (k * T::BN + nc) * 4;
     if (VEC) {
-      const bool in = gk < p.K && gn < p.N;
+      const bool in = gk < p.K && gn < p.N &&
+                      GEMM_IN_EXTENT(static_cast<size_t>(gk) * ldb + gn + 3, b_extent, p.err,
+                                     kSiteBoundsB);
       const float* src = in ? p.B + static_cast<size_t>(gk) * ldb + gn : p.B;
       cp_async_16(dst, src, in ? 16u : 0u);
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool in = gk < p.K && gn + e < p.N;
         const size_t at = trans_b ? static_cast<size_t>(gn + e) * ldb + gk
                                   : static_cast<size_t>(gk) * ldb + gn + e;
+        const bool in = gk < p.K && gn + e < p.N &&
+                        GEMM_IN_EXTENT(at, b_extent, p.err, kSiteBoundsB);
         cp_async_4(dst + 4 * e, in ? p.B + at : p.B, in ? 4u : 0u);
       }
     }
@@ -177,25 +209,30 @@ __device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGenera
 
 // GEN: the general form (row strides, stored transposes, alpha / beta); a
 // separate instantiation, so that the plain product's code is unchanged.
-template <bool VEC, bool GEN>
-__global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams p,
-                                                                const FfmaGeneral gp) {
+template <class T, bool VEC, bool GEN>
+__global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
+    ffma_gemm_kernel(const FfmaParams p, const FfmaGeneral gp) {
+  constexpr int BM = T::BM, BN = T::BN, TY = T::TY, CG = T::CG;
+  // extents (elements) of C and of the partial tiles, for the checked build
+  [[maybe_unused]] const size_t c_extent = stored_extent(p.M, p.N, GEN ? gp.ldc : p.N);
+  [[maybe_unused]] const size_t work_extent =
+      static_cast<size_t>(p.tiles_m * p.tiles_n - p.dp_tiles) * p.max_seg * (BM * BN);
   extern __shared__ __align__(16) float smem_f[];
   __shared__ WorkItem pending[kMaxPending];   // split tiles this CTA must reduce
   __shared__ int pending_count;
-  float* const As = smem_f;                          // [stage][128][kAPitch]
-  float* const Bs = smem_f + kStages * kAStage;      // [stage][16][256]
+  float* const As = smem_f;                          // [stage][BM][kAPitch]
+  float* const Bs = smem_f + kStages * T::A_STAGE;   // [stage][16][BN]
   const uint32_t as_addr = smem_addr(As), bs_addr = smem_addr(Bs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tx = (warp & 1) * 8 + (lane & 7);
-  const int ty = (warp >> 1) * 4 + (lane >> 3);
+  const int tx = (warp % T::WX) * T::LX + lane % T::LX;
+  const int ty = (warp / T::WX) * (32 / T::LX) + lane / T::LX;
   if (threadIdx.x == 0) pending_count = 0;
 
   WorkList list(p);
   WorkItem w;
   while (list.next(p, w)) {
     const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
-    const int m0 = c.tm * kBM, n0 = c.tn * kBN;
+    const int m0 = c.tm * BM, n0 = c.tn * BN;
     const int nk = w.k1 - w.k0;
     // acc[i][q] holds C columns 2q, 2q+1 of row i of this thread's 8 x 16
     uint64_t acc[8][8];
@@ -208,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
 #pragma unroll
     for (int s = 0; s < kStages - 1; ++s) {
       if (s < nk)
-        load_stage<VEC, GEN>(p, gp, m0, n0, w.k0 + s, as_addr + s * kAStage * 4,
-                             bs_addr + s * kBStage * 4);
+        load_stage<T, VEC, GEN>(p, gp, m0, n0, w.k0 + s, as_addr + s * T::A_STAGE * 4,
+                                bs_addr + s * T::B_STAGE * 4);
       cp_async_commit();
     }
 
@@ -219,26 +256,26 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
       const int nxt = j + kStages - 1;
       if (nxt < nk) {
         const int s = nxt % kStages;
-        load_stage<VEC, GEN>(p, gp, m0, n0, w.k0 + nxt, as_addr + s * kAStage * 4,
-                             bs_addr + s * kBStage * 4);
+        load_stage<T, VEC, GEN>(p, gp, m0, n0, w.k0 + nxt, as_addr + s * T::A_STAGE * 4,
+                                bs_addr + s * T::B_STAGE * 4);
       }
       cp_async_commit();
 
-      const float* const as = As + (j % kStages) * kAStage;
-      const float* const bs = Bs + (j % kStages) * kBStage;
+      const float* const as = As + (j % kStages) * T::A_STAGE;
+      const float* const bs = Bs + (j % kStages) * T::B_STAGE;
 #pragma unroll
       for (int kg = 0; kg < kBK / 4; ++kg) {
         float4 a4[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          a4[i] = *reinterpret_cast<const float4*>(as + (ty + 16 * i) * kAPitch + kg * 4);
+          a4[i] = *reinterpret_cast<const float4*>(as + (ty + TY * i) * kAPitch + kg * 4);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           uint64_t b[8];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const ulonglong2 v =
-                *reinterpret_cast<const ulonglong2*>(bs + (kg * 4 + kk) * kBN + g * 64 + tx * 4);
+                *reinterpret_cast<const ulonglong2*>(bs + (kg * 4 + kk) * BN + g * CG + tx * 4);
             b[2 * g] = v.x;
             b[2 * g + 1] = v.y;
           }
@@ -256,25 +293,27 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
     __syncthreads();   // the next item's prologue overwrites stages still being read
 
     if (w.nseg == 1) {
-      // epilogue: rows ty + 16 i, columns 64 g + 4 tx .. +3
+      // epilogue: rows ty + TY i, columns CG g + 4 tx .. +3
       if constexpr (!GEN) {
         const bool c_vec = VEC && (reinterpret_cast<uintptr_t>(p.C) % 16 == 0);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int r = m0 + ty + 16 * i;
+          const int r = m0 + ty + TY * i;
           if (r >= p.M) continue;
           float* crow = p.C + static_cast<size_t>(r) * p.N;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            const int n = n0 + g * 64 + tx * 4;
+            const int n = n0 + g * CG + tx * 4;
             const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
             const float v[4] = {lo.x, lo.y, hi.x, hi.y};
             if (c_vec && n + 3 < p.N) {
-              *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
+              if (GEMM_IN_EXTENT(crow + n + 3 - p.C, c_extent, p.err, kSiteBoundsC))
+                *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
-                if (n + q < p.N) crow[n + q] = v[q];
+                if (n + q < p.N && GEMM_IN_EXTENT(crow + n + q - p.C, c_extent, p.err, kSiteBoundsC))
+                  crow[n + q] = v[q];
             }
           }
         }
@@ -284,27 +323,31 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
         const bool c_vec = VEC && gp.c_vec != 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int r = m0 + ty + 16 * i;
+          const int r = m0 + ty + TY * i;
           if (r >= p.M) continue;
           float* crow = p.C + static_cast<size_t>(r) * gp.ldc;
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            const int n = n0 + g * 64 + tx * 4;
+            const int n = n0 + g * CG + tx * 4;
             const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
             float v[4] = {lo.x, lo.y, hi.x, hi.y};
             if (gp.scale) {
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 v[q] *= gp.alpha;
-                if (gp.beta != 0.0f && n + q < p.N) v[q] = fmaf(gp.beta, crow[n + q], v[q]);
+                if (gp.beta != 0.0f && n + q < p.N &&
+                    GEMM_IN_EXTENT(crow + n + q - p.C, c_extent, p.err, kSiteBoundsC))
+                  v[q] = fmaf(gp.beta, crow[n + q], v[q]);
               }
             }
             if (c_vec && n + 3 < p.N) {
-              *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
+              if (GEMM_IN_EXTENT(crow + n + 3 - p.C, c_extent, p.err, kSiteBoundsC))
+                *reinterpret_cast<float4*>(crow + n) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
 #pragma unroll
               for (int q = 0; q < 4; ++q)
-                if (n + q < p.N) crow[n + q] = v[q];
+                if (n + q < p.N && GEMM_IN_EXTENT(crow + n + q - p.C, c_extent, p.err, kSiteBoundsC))
+                  crow[n + q] = v[q];
             }
           }
         }
@@ -313,14 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
       // part of a split tile: publish it; the CTA that publishes last reduces
       // the tile after its work list
       float* const slot =
-          p.partials + (static_cast<size_t>(w.tail) * p.max_seg + w.seg) * (kBM * kBN);
+          p.partials + (static_cast<size_t>(w.tail) * p.max_seg + w.seg) * (BM * BN);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const float2 lo = unpair(acc[i][2 * g]), hi = unpair(acc[i][2 * g + 1]);
-          *reinterpret_cast<float4*>(slot + (ty + 16 * i) * kBN + g * 64 + tx * 4) =
-              make_float4(lo.x, lo.y, hi.x, hi.y);
+          float* const to = slot + (ty + TY * i) * BN + g * CG + tx * 4;
+          if (GEMM_IN_EXTENT(to + 3 - p.partials, work_extent, p.err, kSiteBoundsWork))
+            *reinterpret_cast<float4*>(to) = make_float4(lo.x, lo.y, hi.x, hi.y);
         }
       }
       __threadfence();
@@ -343,14 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
     for (int e = 0; e < npend; ++e) {
       const WorkItem pw = pending[e];
       const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
-      const float* parts = p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (kBM * kBN);
+      const size_t at = static_cast<size_t>(pw.tail) * p.max_seg * (BM * BN);
+      const float* parts = p.partials + at;
+      const BoundsRef br{p.err, work_extent - at, c_extent};
       if constexpr (!GEN)
-        reduce_partials<kBM, kBN, kThreads, 8>(parts, pw.nseg, c.tm * kBM, c.tn * kBN, p.M, p.N,
-                                               p.C);
+        reduce_partials<BM, BN, T::THREADS, 8>(parts, pw.nseg, c.tm * BM, c.tn * BN, p.M, p.N,
+                                               p.C, br);
       else
-        reduce_partials_general<kBM, kBN, kThreads, 8>(parts, pw.nseg, c.tm * kBM, c.tn * kBN,
+        reduce_partials_general<BM, BN, T::THREADS, 8>(parts, pw.nseg, c.tm * BM, c.tn * BN,
                                                        p.M, p.N, p.C, gp.ldc, gp.scale, gp.alpha,
-                                                       gp.beta);
+                                                       gp.beta, br);
     }
   }
   if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
@@ -358,27 +404,43 @@ __global__ void __launch_bounds__(kThreads, 1) ffma_gemm_kernel(const FfmaParams
 
 constexpr int kMaxDevices = 64;
 
-template <bool VEC, bool GEN>
-int launch_vec(const GemmArgs& g, const FfmaParams& p, const FfmaGeneral& gp, int grid,
-               cudaStream_t stream) {
-  static std::atomic<unsigned long long> configured{0};  // bit per device
-  const unsigned long long bit = 1ull << (g.device % kMaxDevices);
-  if (!(configured.load() & bit)) {
-    if (cudaFuncSetAttribute(ffma_gemm_kernel<VEC, GEN>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess) {
-      (void)cudaGetLastError();
-      return GEMM_F32_ELAUNCH;
-    }
-    configured.fetch_or(bit);
+// Configures the kernel once per device (its dynamic shared memory, and all
+// of the unified L1 / shared memory as shared memory: two CTAs of the
+// 128-thread tiles, 96 KB each, fit on an SM only with it) and returns how
+// many of its CTAs an SM holds (0 on failure).
+template <class T, bool VEC, bool GEN>
+int resident_ctas(int device) {
+  static std::atomic<int> per_sm[kMaxDevices];   // 0: not configured yet
+  const int d = device % kMaxDevices;
+  int n = per_sm[d].load();
+  if (n > 0) return n;
+  auto kern = ffma_gemm_kernel<T, VEC, GEN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::THREADS, T::SMEM) != cudaSuccess ||
+      n < 1) {
+    (void)cudaGetLastError();
+    return 0;
   }
-  ffma_gemm_kernel<VEC, GEN><<<grid, kThreads, kSmemBytes, stream>>>(p, gp);
+  n = std::min(n, T::CTAS_PER_SM);
+  per_sm[d].store(n);
+  return n;
+}
+
+template <class T, bool VEC, bool GEN>
+int launch_vec(const FfmaParams& p, const FfmaGeneral& gp, int grid, cudaStream_t stream) {
+  ffma_gemm_kernel<T, VEC, GEN><<<grid, T::THREADS, T::SMEM, stream>>>(p, gp);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;
 }
 
-}  // namespace
-
-int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
+// Plans and launches the product on block tiles T: persistent CTAs
+// (CTAS_PER_SM per SM), the last partial wave split along K when that
+// leaves every CTA at least kMinSplitItersFfma K tiles.
+template <class T>
+int launch_tile(GemmArgs& g, cudaStream_t stream, int* launches) {
   *launches = 0;
   FfmaParams p;
   p.A = g.A;
@@ -387,8 +449,8 @@ int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
   p.M = g.M;
   p.N = g.N;
   p.K = g.K;
-  p.tiles_m = (g.M + kBM - 1) / kBM;
-  p.tiles_n = (g.N + kBN - 1) / kBN;
+  p.tiles_m = (g.M + T::BM - 1) / T::BM;
+  p.tiles_n = (g.N + T::BN - 1) / T::BN;
   p.k_iters = (g.K + kBK - 1) / kBK;
   p.partials = nullptr;
   p.counters = nullptr;
@@ -409,36 +471,54 @@ int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
   p.sk_ctas = 0;
   p.sk_work = 0;
   p.max_seg = 1;
+  // 16-byte copies: untransposed, strides a multiple of 4 floats, aligned
+  // bases, and K, N multiples of 4 (a chunk is wholly inside or outside)
+  const bool vec = tma_addressable(g) && g.K % 4 == 0 && g.N % 4 == 0;
+  const bool gen = !plain_form(g);
+  const int per_sm = gen ? (vec ? resident_ctas<T, true, true>(g.device)
+                                : resident_ctas<T, false, true>(g.device))
+                         : (vec ? resident_ctas<T, true, false>(g.device)
+                                : resident_ctas<T, false, false>(g.device));
+  if (per_sm < 1) return GEMM_F32_ELAUNCH;
+  const int slots = g.num_sms * per_sm;   // CTAs resident at once
   int grid = (g.flags & GEMM_F32_FLAG_ONE_TILE_PER_CTA)
                  ? static_cast<int>(tiles)
-                 : static_cast<int>(std::min<long>(tiles, g.num_sms));
+                 : static_cast<int>(std::min<long>(tiles, slots));
   if (!(g.flags & (GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K))) {
     FfmaParams q = p;
     const size_t ws_bytes =
-        plan_split_tail(q, tiles, g.num_sms, sizeof(float) * kBM * kBN, kMinSplitItersFfma);
+        plan_split_tail(q, tiles, slots, sizeof(float) * T::BM * T::BN, kMinSplitItersFfma);
     void* ws = ws_bytes ? acquire_workspace(g.device, stream, ws_bytes) : nullptr;
     if (ws) {
       p = q;
-      grid = g.num_sms;
+      grid = slots;
       p.counters = static_cast<unsigned long long*>(ws);
       p.partials = reinterpret_cast<float*>(static_cast<char*>(ws) + kCounterBytes);
     }
   }
-  // 16-byte copies: untransposed, strides a multiple of 4 floats, aligned
-  // bases, and K, N multiples of 4 (a chunk is wholly inside or outside)
-  const bool vec = tma_addressable(g) && g.K % 4 == 0 && g.N % 4 == 0;
   int rc;
-  if (!plain_form(g))
-    rc = vec ? launch_vec<true, true>(g, p, gp, grid, stream)
-             : launch_vec<false, true>(g, p, gp, grid, stream);
+  if (gen)
+    rc = vec ? launch_vec<T, true, true>(p, gp, grid, stream)
+             : launch_vec<T, false, true>(p, gp, grid, stream);
   else
-    rc = vec ? launch_vec<true, false>(g, p, gp, grid, stream)
-             : launch_vec<false, false>(g, p, gp, grid, stream);
+    rc = vec ? launch_vec<T, true, false>(p, gp, grid, stream)
+             : launch_vec<T, false, false>(p, gp, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "ffma_gemm_kernel";
   }
   return rc;
+}
+
+}  // namespace
+
+// Block tiles by shape: a tile taller than wide for N <= 64 and one wider
+// than tall for M <= 64, where the 128 x 256 tile would spend three quarters
+// (N = 64) or half (M = 64) of its multiply-adds beyond the matrix.
+int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches) {
+  if (g.N <= TileTall::BN && g.M > TileShort::BM) return launch_tile<TileTall>(g, stream, launches);
+  if (g.M <= TileShort::BM) return launch_tile<TileShort>(g, stream, launches);
+  return launch_tile<TileWide>(g, stream, launches);
 }
 
 }  // namespace gemm_f32_impl

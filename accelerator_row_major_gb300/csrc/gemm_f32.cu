@@ -13,6 +13,7 @@
 #include <unordered_map>
 
 #include "../../include/gemm_f32.h"
+#include "device_common.cuh"
 #include "launch.h"
 
 namespace {
@@ -110,7 +111,8 @@ bool overlaps(const void* a, size_t a_bytes, const void* b, size_t b_bytes) {
 }
 
 constexpr unsigned kKnownFlags = GEMM_F32_FLAG_FORCE_STAGED | GEMM_F32_FLAG_TILE64 |
-                                 GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
+                                 GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE224 |
+                                 GEMM_F32_FLAG_TILE256 |
                                  GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K |
                                  GEMM_F32_FLAG_CTA_PAIR | GEMM_F32_FLAG_SINGLE_CTA |
                                  GEMM_F32_FLAG_TEST_DROP_COPY;
@@ -167,20 +169,25 @@ int check_operands(const float* A, const float* B, const float* C, int M, int N,
 // C = beta * C over an M x N window with row stride ldc (C = 0 when beta
 // is 0, without reading C).  The general form's case of an empty or
 // zero-weighted product.
-__global__ void scale_window_kernel(float* C, int M, int N, int ldc, float beta) {
+__global__ void scale_window_kernel(float* C, int M, int N, int ldc, float beta, unsigned* err) {
   const long long total = static_cast<long long>(M) * N;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
        t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    float* c = C + (t / N) * static_cast<long long>(ldc) + t % N;
+    const long long at = (t / N) * static_cast<long long>(ldc) + t % N;
+    if (!GEMM_IN_EXTENT(at, gemm_f32_dev::stored_extent(M, N, ldc), err,
+                        gemm_f32_dev::kSiteBoundsC))
+      continue;
+    float* c = C + at;
     *c = beta != 0.0f ? beta * *c : 0.0f;
   }
 }
 
-int scale_window(float* C, int M, int N, int ldc, float beta, int num_sms, cudaStream_t stream) {
+int scale_window(float* C, int M, int N, int ldc, float beta, int num_sms, unsigned* err,
+                 cudaStream_t stream) {
   const long long total = static_cast<long long>(M) * N;
   const long long want = (total + 255) / 256;
   const int grid = static_cast<int>(want < 4LL * num_sms ? want : 4LL * num_sms);
-  scale_window_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, beta);
+  scale_window_kernel<<<grid, 256, 0, stream>>>(C, M, N, ldc, beta, err);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   t_last_launches = 1;
   t_last_kernel = "scale_window_kernel";
@@ -233,7 +240,8 @@ extern "C" int gemm_f32_ex(const float* A, const float* B, float* C, int M, int 
   if (mode != GEMM_F32_MODE_TC3X && mode != GEMM_F32_MODE_FFMA && mode != GEMM_F32_MODE_TC1X)
     return GEMM_F32_EINVAL;
   if (flags & ~kKnownFlags) return GEMM_F32_EINVAL;
-  const unsigned bn_flags = flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256);
+  const unsigned bn_flags = flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 |
+                                     GEMM_F32_FLAG_TILE224 | GEMM_F32_FLAG_TILE256);
   if (bn_flags & (bn_flags - 1)) return GEMM_F32_EINVAL;  // at most one tile width
   if ((flags & GEMM_F32_FLAG_CTA_PAIR) && (flags & GEMM_F32_FLAG_SINGLE_CTA)) return GEMM_F32_EINVAL;
   const int chk = check_operands(A, B, C, M, N, K);
@@ -351,7 +359,7 @@ extern "C" int gemm_f32_general(int trans_a, int trans_b, int M, int N, int K, f
   DeviceState* st = device_state(&dev);
   if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_handle);
-  if (!use_ab) return scale_window(C, M, N, ldc, beta, st->num_sms, stream);
+  if (!use_ab) return scale_window(C, M, N, ldc, beta, st->num_sms, st->err, stream);
 
   gemm_f32_impl::GemmArgs g;
   g.A = A;
@@ -608,4 +616,10 @@ extern "C" int gemm_f32_last_launches(void) { return t_last_launches; }
 
 extern "C" const char* gemm_f32_last_kernel(void) { return t_last_kernel; }
 
-extern "C" const char* gemm_f32_version(void) { return "gemm_f32 1.0 sm_103a"; }
+extern "C" const char* gemm_f32_version(void) {
+#ifdef GEMM_BOUNDS_CHECK
+  return "gemm_f32 1.0 sm_103a bounds-checked";
+#else
+  return "gemm_f32 1.0 sm_103a";
+#endif
+}

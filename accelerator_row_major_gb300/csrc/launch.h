@@ -81,7 +81,7 @@ int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches);
 // its kernels in *launches.
 constexpr long long kPackMinWork = 1LL << 27;
 int pack_operand(const float* src, int rows, int cols, int ld_src, bool transposed, float* dst,
-                 int ld_dst, int num_sms, cudaStream_t stream);
+                 int ld_dst, int num_sms, unsigned* err, cudaStream_t stream);
 int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches);
 
 // The library's pack buffer for `stream` on `device`, grown to at least

@@ -19,9 +19,11 @@
 #include <cstdint>
 
 #include "../../include/gemm_f32.h"
+#include "device_common.cuh"
 #include "launch.h"
 
 namespace gemm_f32_impl {
+using namespace gemm_f32_dev;
 
 namespace {
 
@@ -34,7 +36,16 @@ struct RowCopy {
   int rows, cols;
 };
 
-__global__ void pack_rows_kernel(RowCopy x, RowCopy y) {
+// Extents (elements) of one copy's source and destination windows, for the
+// checked build.
+__device__ __forceinline__ size_t src_extent(const RowCopy& m) {
+  return stored_extent(m.rows, m.cols, m.ld_src);
+}
+__device__ __forceinline__ size_t dst_extent(const RowCopy& m) {
+  return stored_extent(m.rows, m.cols, m.ld_dst);
+}
+
+__global__ void pack_rows_kernel(RowCopy x, RowCopy y, unsigned* err) {
   const long long nx = static_cast<long long>(x.rows) * x.cols;
   const long long total = nx + static_cast<long long>(y.rows) * y.cols;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
@@ -45,15 +56,20 @@ __global__ void pack_rows_kernel(RowCopy x, RowCopy y) {
     const long long r = e / cols, c = e % cols;
     const float* const src = in_x ? x.src : y.src;
     float* const dst = in_x ? x.dst : y.dst;
-    dst[r * (in_x ? x.ld_dst : y.ld_dst) + c] = __ldg(src + r * (in_x ? x.ld_src : y.ld_src) + c);
+    const long long is = r * (in_x ? x.ld_src : y.ld_src) + c;
+    const long long id = r * (in_x ? x.ld_dst : y.ld_dst) + c;
+    if (GEMM_IN_EXTENT(is, src_extent(in_x ? x : y), err, kSiteBoundsPack) &&
+        GEMM_IN_EXTENT(id, dst_extent(in_x ? x : y), err, kSiteBoundsPack))
+      dst[id] = __ldg(src + is);
   }
 }
 
-int launch_rows(const RowCopy& x, const RowCopy& y, int num_sms, cudaStream_t stream) {
+int launch_rows(const RowCopy& x, const RowCopy& y, int num_sms, unsigned* err,
+                cudaStream_t stream) {
   const long long total = static_cast<long long>(x.rows) * x.cols + static_cast<long long>(y.rows) * y.cols;
   const long long want = (total + 255) / 256;
   const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-  pack_rows_kernel<<<grid, 256, 0, stream>>>(x, y);
+  pack_rows_kernel<<<grid, 256, 0, stream>>>(x, y, err);
   return cudaGetLastError() == cudaSuccess ? GEMM_F32_OK : GEMM_F32_ELAUNCH;
 }
 
@@ -70,34 +86,42 @@ RowCopy row_copy(const float* src, int rows, int cols, int ld_src, float* dst, i
 
 // block (32, 8): tile (blockIdx.y, blockIdx.x) of dst, rows r0.., cols c0..
 __global__ void pack_transpose_kernel(const float* __restrict__ src, int rows, int cols,
-                                      long long ld_src, float* __restrict__ dst, long long ld_dst) {
+                                      long long ld_src, float* __restrict__ dst, long long ld_dst,
+                                      unsigned* err) {
   __shared__ float tile[kTile][kTile + 1];
   const int r0 = blockIdx.y * kTile, c0 = blockIdx.x * kTile;
   // read src rows c0.. (dst columns), lanes along src columns (dst rows)
   for (int y = threadIdx.y; y < kTile; y += blockDim.y) {
     const int c = c0 + y, r = r0 + threadIdx.x;
-    if (c < cols && r < rows) tile[y][threadIdx.x] = __ldg(src + static_cast<long long>(c) * ld_src + r);
+    if (c < cols && r < rows &&
+        GEMM_IN_EXTENT(static_cast<long long>(c) * ld_src + r, stored_extent(cols, rows, ld_src), err,
+                       kSiteBoundsPack))
+      tile[y][threadIdx.x] = __ldg(src + static_cast<long long>(c) * ld_src + r);
   }
   __syncthreads();
   for (int y = threadIdx.y; y < kTile; y += blockDim.y) {
     const int r = r0 + y, c = c0 + threadIdx.x;
-    if (r < rows && c < cols) dst[static_cast<long long>(r) * ld_dst + c] = tile[threadIdx.x][y];
+    if (r < rows && c < cols &&
+        GEMM_IN_EXTENT(static_cast<long long>(r) * ld_dst + c, stored_extent(rows, cols, ld_dst), err,
+                       kSiteBoundsPack))
+      dst[static_cast<long long>(r) * ld_dst + c] = tile[threadIdx.x][y];
   }
 }
 
 }  // namespace
 
 int pack_operand(const float* src, int rows, int cols, int ld_src, bool transposed, float* dst,
-                 int ld_dst, int num_sms, cudaStream_t stream) {
+                 int ld_dst, int num_sms, unsigned* err, cudaStream_t stream) {
   if (rows <= 0 || cols <= 0) return GEMM_F32_OK;
   if (!transposed) {
     return launch_rows(row_copy(src, rows, cols, ld_src, dst, ld_dst),
-                       row_copy(src, 0, 1, ld_src, dst, ld_dst), num_sms, stream);
+                       row_copy(src, 0, 1, ld_src, dst, ld_dst), num_sms, err, stream);
   } else {
     const long long gy = (rows + kTile - 1) / kTile;
     if (gy > 65535) return GEMM_F32_EINVAL;
     const dim3 grid((cols + kTile - 1) / kTile, static_cast<unsigned>(gy));
-    pack_transpose_kernel<<<grid, dim3(kTile, 8), 0, stream>>>(src, rows, cols, ld_src, dst, ld_dst);
+    pack_transpose_kernel<<<grid, dim3(kTile, 8), 0, stream>>>(src, rows, cols, ld_src, dst, ld_dst,
+                                                              err);
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;
@@ -118,7 +142,8 @@ int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches) {
   if (pack_a && pack_b && !g.trans_a && !g.trans_b) {
     // both plain row copies: one launch
     const int rc = launch_rows(row_copy(g.A, g.M, g.K, g.lda, buf, lda),
-                               row_copy(g.B, g.K, g.N, g.ldb, b_dst, ldb), g.num_sms, stream);
+                               row_copy(g.B, g.K, g.N, g.ldb, b_dst, ldb), g.num_sms, g.err,
+                               stream);
     if (rc != GEMM_F32_OK) return rc;
     g.A = buf;
     g.lda = lda;
@@ -128,7 +153,8 @@ int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches) {
     return GEMM_F32_OK;
   }
   if (pack_a) {
-    const int rc = pack_operand(g.A, g.M, g.K, g.lda, g.trans_a != 0, buf, lda, g.num_sms, stream);
+    const int rc =
+        pack_operand(g.A, g.M, g.K, g.lda, g.trans_a != 0, buf, lda, g.num_sms, g.err, stream);
     if (rc != GEMM_F32_OK) return rc;
     g.A = buf;
     g.lda = lda;
@@ -136,7 +162,8 @@ int pack_for_tma(GemmArgs& g, cudaStream_t stream, int* launches) {
     ++*launches;
   }
   if (pack_b) {
-    const int rc = pack_operand(g.B, g.K, g.N, g.ldb, g.trans_b != 0, b_dst, ldb, g.num_sms, stream);
+    const int rc =
+        pack_operand(g.B, g.K, g.N, g.ldb, g.trans_b != 0, b_dst, ldb, g.num_sms, g.err, stream);
     if (rc != GEMM_F32_OK) return rc;
     g.B = b_dst;
     g.ldb = ldb;

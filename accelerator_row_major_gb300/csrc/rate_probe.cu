@@ -31,6 +31,7 @@ constexpr int kMmaM = 128, kMmaN = 256, kMmaK = 8;
 constexpr int kBRows = kMmaN;           // shared-memory operand: 256 rows x 8 k (64-byte swizzle atoms)
 constexpr int kFfmaThreads = 512;
 constexpr int kFfmaChains = 8;          // independent fma.rn.f32x2 chains per thread
+constexpr int kFfmaUnroll = 32;         // chain steps per loop iteration (loop overhead < 1 %)
 
 struct ProbeOut {
   unsigned long long cycles;   // SM clock cycles of this CTA's timed work
@@ -188,7 +189,7 @@ __global__ void __launch_bounds__(kFfmaThreads, 1) ffma_rate_kernel(ProbeOut* ou
 #pragma unroll 1
   for (int i = 0; i < iters; ++i) {
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
+    for (int u = 0; u < kFfmaUnroll; ++u)
 #pragma unroll
       for (int j = 0; j < kFfmaChains; ++j) acc[j] = probe_fma2(acc[j], m, c);
   }
@@ -259,7 +260,7 @@ int unit_rates(gemm_f32_unit_rates_t* r) {
   ProbeOut* const d_out = static_cast<ProbeOut*>(buf);
   unsigned* const d_err = reinterpret_cast<unsigned*>(static_cast<char*>(buf) + out_bytes);
   float* const d_sink = reinterpret_cast<float*>(static_cast<char*>(buf) + out_bytes + 256);
-  const int mma_iters = 8192, ffma_iters = 4096;
+  const int mma_iters = 8192, ffma_iters = 512;
   const int pair_grid = sms & ~1;
   double mhz_tf32 = 0, mhz_pair = 0, mhz_ffma = 0;
   int rc = run_probe(
@@ -287,7 +288,7 @@ int unit_rates(gemm_f32_unit_rates_t* r) {
   if (rc == GEMM_F32_OK)
     rc = run_probe(
         [&] { ffma_rate_kernel<<<sms, kFfmaThreads>>>(d_out, d_sink, ffma_iters); }, sms, 1,
-        4.0 * kFfmaThreads * kFfmaChains * 4.0 * ffma_iters, d_out, d_err,
+        4.0 * kFfmaThreads * kFfmaChains * kFfmaUnroll * ffma_iters, d_out, d_err,
         &r->ffma_flop_per_clk_sm, &mhz_ffma);
   (void)cudaFree(buf);
   if (rc != GEMM_F32_OK) {

@@ -17,9 +17,11 @@
 #include <cstdint>
 
 #include "../../include/gemm_f32.h"
+#include "device_common.cuh"
 #include "launch.h"
 
 namespace gemm_f32_impl {
+using namespace gemm_f32_dev;
 
 namespace {
 
@@ -28,7 +30,7 @@ constexpr int kT = 16;
 __global__ void __launch_bounds__(kT * kT) small_gemm_kernel(const float* __restrict__ A,
                                                              const float* __restrict__ B,
                                                              float* __restrict__ C, int M, int N,
-                                                             int K) {
+                                                             int K, unsigned* err) {
   __shared__ float as[kT][kT];
   __shared__ float bs[kT][kT];
   const int tx = threadIdx.x, ty = threadIdx.y;
@@ -36,14 +38,24 @@ __global__ void __launch_bounds__(kT * kT) small_gemm_kernel(const float* __rest
   const int j = blockIdx.x * kT + tx;
   float acc = 0.0f;
   for (int k0 = 0; k0 < K; k0 += kT) {
-    as[ty][tx] = (i < M && k0 + tx < K) ? __ldg(A + static_cast<size_t>(i) * K + k0 + tx) : 0.0f;
-    bs[ty][tx] = (k0 + ty < K && j < N) ? __ldg(B + static_cast<size_t>(k0 + ty) * N + j) : 0.0f;
+    const size_t ia = static_cast<size_t>(i) * K + k0 + tx;
+    const size_t ib = static_cast<size_t>(k0 + ty) * N + j;
+    as[ty][tx] = (i < M && k0 + tx < K &&
+                  GEMM_IN_EXTENT(ia, static_cast<size_t>(M) * K, err, kSiteBoundsA))
+                     ? __ldg(A + ia)
+                     : 0.0f;
+    bs[ty][tx] = (k0 + ty < K && j < N &&
+                  GEMM_IN_EXTENT(ib, static_cast<size_t>(K) * N, err, kSiteBoundsB))
+                     ? __ldg(B + ib)
+                     : 0.0f;
     __syncthreads();
 #pragma unroll
     for (int k = 0; k < kT; ++k) acc = fmaf(as[ty][k], bs[k][tx], acc);
     __syncthreads();
   }
-  if (i < M && j < N) C[static_cast<size_t>(i) * N + j] = acc;
+  if (i < M && j < N &&
+      GEMM_IN_EXTENT(static_cast<size_t>(i) * N + j, static_cast<size_t>(M) * N, err, kSiteBoundsC))
+    C[static_cast<size_t>(i) * N + j] = acc;
 }
 
 }  // namespace
@@ -56,7 +68,7 @@ bool small_suits(const GemmArgs& g) {
 int launch_small(GemmArgs& g, cudaStream_t stream, int* launches) {
   *launches = 0;
   const dim3 grid((g.N + kT - 1) / kT, (g.M + kT - 1) / kT);
-  small_gemm_kernel<<<grid, dim3(kT, kT), 0, stream>>>(g.A, g.B, g.C, g.M, g.N, g.K);
+  small_gemm_kernel<<<grid, dim3(kT, kT), 0, stream>>>(g.A, g.B, g.C, g.M, g.N, g.K, g.err);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   *launches = 1;
   g.kernel = "small_gemm_kernel";

@@ -146,7 +146,7 @@ struct TcCfg {
   static constexpr bool STACK = TM == 64 && NPROD == 3 && !LSTACK;
   static constexpr int MMA_M = LSTACK ? 128 : TN;                   // TMEM lanes of the MMA
   static constexpr int ACC_W = STACK ? 2 * TM : TM;                 // columns per accumulator
-  static constexpr int NACC = (TM == 256 || STACK) ? 1 : 2;         // accumulators in TMEM
+  static constexpr int NACC = (TM >= 224 || STACK) ? 1 : 2;         // accumulators in TMEM
   static constexpr int ACC_COLS = NACC * ACC_W;
   static constexpr int BT_COLS = (NPROD == 3 && !LSTACK) ? 2 * BK : BK;   // B^T columns per stage
   static constexpr int XCHG_BYTES = LSTACK ? 64 * 33 * 4 : 0;       // epilogue exchange buffer
@@ -160,7 +160,7 @@ struct TcCfg {
   static constexpr uint32_t A_SBO = BK == 32 ? 1024u : 512u;       // 8-row group stride
   static_assert(STAGES >= 2, "at least two stages");
   static_assert(BK == 16 || BK == 32, "BK");
-  static_assert(TM == 64 || TM == 128 || TM == 256, "TM");
+  static_assert(TM == 64 || TM == 128 || TM == 224 || TM == 256, "TM");
   static_assert(A_BYTES % 1024 == 0 && STAGE_BYTES % 1024 == 0, "1024-byte aligned atoms");
   static_assert(ACC_COLS + STAGES * BT_COLS <= kTmemCols, "TMEM budget");
 };
@@ -239,6 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
   using Cfg = TcCfg<TM, BK, NPROD, TN>;
   static_assert(TN == kTN || (TN == kTNNarrow && LOAD == kLoadTma), "narrow tiles: TMA only");
+  // extents (elements) of the arrays indexed by hand, for the checked build
+  [[maybe_unused]] const size_t a_extent =
+      trans_a ? stored_extent(p.K, p.M, lda) : stored_extent(p.M, p.K, lda);
+  [[maybe_unused]] const size_t b_extent =
+      trans_b ? stored_extent(p.N, p.K, ldb) : stored_extent(p.K, p.N, ldb);
+  [[maybe_unused]] const size_t c_extent = stored_extent(p.M, p.N, ldc);
+  [[maybe_unused]] const size_t work_extent =
+      static_cast<size_t>(p.tiles_m * p.tiles_n - p.dp_tiles) * p.max_seg * (TM * TN);
   constexpr int S = Cfg::STAGES;
   constexpr int NACC = Cfg::NACC;
   extern __shared__ uint8_t smem_dyn[];
@@ -453,7 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_rows(chunk, v);
           if (live) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * TN] = __uint_as_float(v[j]);
+            for (int j = 0; j < 32; ++j)
+              if (GEMM_IN_EXTENT(mine + (chunk * 32 + j) * TN - p.partials, work_extent, p.err,
+                                 kSiteBoundsWork))
+                mine[(chunk * 32 + j) * TN] = __uint_as_float(v[j]);
           }
         }
         __threadfence();
@@ -478,11 +489,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!scale) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (j < rows) dst[static_cast<size_t>(j) * ldc] = __uint_as_float(v[j]);
+                if (j < rows && GEMM_IN_EXTENT(dst + static_cast<size_t>(j) * ldc - p.C, c_extent,
+                                               p.err, kSiteBoundsC))
+                  dst[static_cast<size_t>(j) * ldc] = __uint_as_float(v[j]);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                if (j < rows) {
+                if (j < rows &&
+                    GEMM_IN_EXTENT(dst + static_cast<size_t>(j) * ldc - p.C, c_extent, p.err,
+                                   kSiteBoundsC)) {
                   float* d = dst + static_cast<size_t>(j) * ldc;
                   *d = scaled_c(__uint_as_float(v[j]), d, gp.alpha, gp.beta);
                 }
@@ -575,7 +590,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int gm = m0 + r, gk = k0 + k;
               const size_t at = trans_a ? static_cast<size_t>(gk) * lda + gm
                                           : static_cast<size_t>(gm) * lda + gk;
-              av[j] = (gm < p.M && gk < p.K) ? __float_as_uint(__ldg(p.A + at)) : 0u;
+              av[j] = (gm < p.M && gk < p.K &&
+                       GEMM_IN_EXTENT(at, a_extent, p.err, kSiteBoundsA))
+                          ? __float_as_uint(__ldg(p.A + at))
+                          : 0u;
             }
             if (c0 == 0) {
               // B tile: column n0 + col, K rows of this thread's half (lanes along n)
@@ -584,7 +602,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int gk = k0 + kh0 + k;
                 const size_t bt_at = trans_b ? static_cast<size_t>(gn) * ldb + gk
                                                : static_cast<size_t>(gk) * ldb + gn;
-                bv[k] = (gn < p.N && gk < p.K) ? __float_as_uint(__ldg(p.B + bt_at)) : 0u;
+                bv[k] = (gn < p.N && gk < p.K &&
+                         GEMM_IN_EXTENT(bt_at, b_extent, p.err, kSiteBoundsB))
+                            ? __float_as_uint(__ldg(p.B + bt_at))
+                            : 0u;
               }
             }
 #pragma unroll
@@ -648,20 +669,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.partials + static_cast<size_t>(pw.tail) * p.max_seg * (TM * TN));
       constexpr int kVec = TM * TN / 4;           // float4s per partial
       constexpr int kPer = kVec / kThreads;       // per thread
+      constexpr int kH = (kPer + 1) / 2;          // per thread and half (the last may be short)
+      static_assert(kVec % kThreads == 0, "partial tile shape");
 #pragma unroll 1
       for (int half = 0; half < 2; ++half) {
-        float4 sum[kPer / 2];
+        float4 sum[kH];
 #pragma unroll
-        for (int i = 0; i < kPer / 2; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < kH; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
         for (int sg = 0; sg < pw.nseg; ++sg) {
-          float4 x[kPer / 2];
+          float4 x[kH];
 #pragma unroll
-          for (int i = 0; i < kPer / 2; ++i)
-            x[i] = __ldcg(parts + static_cast<size_t>(sg) * kVec + threadIdx.x +
-                          (half * (kPer / 2) + i) * kThreads);
+          for (int i = 0; i < kH; ++i) {
+            if (half * kH + i >= kPer) {
+              x[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+              continue;
+            }
+            const size_t f4 = static_cast<size_t>(sg) * kVec + threadIdx.x +
+                              (half * kH + i) * kThreads;
+            x[i] = GEMM_IN_EXTENT(
+                       4 * (f4 + (parts - reinterpret_cast<const float4*>(p.partials))) + 3,
+                       work_extent, p.err, kSiteBoundsWork)
+                       ? __ldcg(parts + f4)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
 #pragma unroll
-          for (int i = 0; i < kPer / 2; ++i) {
+          for (int i = 0; i < kH; ++i) {
             sum[i].x += x[i].x;
             sum[i].y += x[i].y;
             sum[i].z += x[i].z;
@@ -669,8 +702,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
 #pragma unroll
-        for (int i = 0; i < kPer / 2; ++i) {
-          const int f = threadIdx.x + (half * (kPer / 2) + i) * kThreads;  // float4 index
+        for (int i = 0; i < kH; ++i) {
+          if (half * kH + i >= kPer) continue;
+          const int f = threadIdx.x + (half * kH + i) * kThreads;  // float4 index
           const int m = c.tm * TM + f / (TN / 4);
           const int n = c.tn * TN + (f % (TN / 4)) * 4;
           if (m < p.M) {
@@ -678,7 +712,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float vals[4] = {sum[i].x, sum[i].y, sum[i].z, sum[i].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (n + q < p.N) dst[q] = scale ? scaled_c(vals[q], dst + q, gp.alpha, gp.beta) : vals[q];
+              if (n + q < p.N &&
+                  GEMM_IN_EXTENT(dst + q - p.C, c_extent, p.err, kSiteBoundsC))
+                dst[q] = scale ? scaled_c(vals[q], dst + q, gp.alpha, gp.beta) : vals[q];
           }
         }
       }
@@ -748,6 +784,10 @@ int launch_tm(int tm, const GemmArgs& g, const TcParams& p, const TcGeneral& gp,
   switch (tm) {
     case 64: return launch_one<64, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
     case 128: return launch_one<128, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
+    case 224:
+      if constexpr (LOAD == kLoadTma)
+        return launch_one<224, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
+      return GEMM_F32_EINVAL;
     default: return launch_one<256, BK, NPROD, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
   }
 }
@@ -763,10 +803,13 @@ int launch_tm_bk(int tm, int bk, const GemmArgs& g, const TcParams& p, const TcG
       if (bk == 16) return launch_tm<16, 1, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
     return launch_tm<32, 1, LOAD, TN>(tm, g, p, gp, ma, mb, grid, stream);
   }
-  // three products take 16-deep stages only with 256-row tiles (bk_for)
-  if (bk == 16)
+  // three products take 16-deep stages only with 224- and 256-row tiles (bk_for)
+  if (bk == 16) {
+    if constexpr (LOAD == kLoadTma)
+      if (tm == 224) return launch_one<224, 16, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
     return tm == 256 ? launch_one<256, 16, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream)
                      : GEMM_F32_EINVAL;
+  }
   return tm == 64 ? launch_one<64, 32, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream)
                   : launch_one<128, 32, 3, LOAD, TN>(g, p, gp, ma, mb, grid, stream);
 }
@@ -809,24 +852,28 @@ TcGeneral general_of(const GemmArgs& g) {
 
 // Tile height TM.  With the split tail the schedule no longer quantises to
 // whole waves, so the most efficient height is used (256; 128 or 64 when M
-// is that small).  Without it (ONE_TILE_PER_CTA or NO_SPLIT_K), the height
-// whose schedule gives the busiest SM the least time: rounds of tiles x TM /
-// (relative efficiency), the efficiencies being measured throughputs of
-// TM = 128 and 64 relative to TM = 256: 8192^3 for tiles 128 columns wide,
-// 65536 x 1024 x 64 and 131072 x 1024 x 64 for narrow ones (where 128-row
-// tiles cost 4 % more per row than 256-row ones).
-int choose_tm(const GemmArgs& g, bool split_tail, int width) {
+// is that small).  Without it (too few K iterations to split, ONE_TILE_PER_CTA
+// or NO_SPLIT_K), the height whose schedule gives the busiest SM the least
+// time: rounds of tiles x TM / (relative efficiency), the efficiencies being
+// measured throughputs of TM = 224, 128 and 64 relative to TM = 256: 8192^3
+// for tiles 128 columns wide, 65536 x 1024 x 64 and 131072 x 1024 x 64 for
+// narrow ones (where 128-row tiles cost 4 % more per row than 256-row ones).
+// 224-row tiles exist on the TMA path only; they turn 1.68 waves of 256-row
+// tiles (65536 rows on 152 SMs) into two nearly full ones.
+int choose_tm(const GemmArgs& g, bool split_tail, int width, bool tma) {
   if (g.flags & GEMM_F32_FLAG_TILE64) return 64;
   if (g.flags & GEMM_F32_FLAG_TILE128) return 128;
+  if (g.flags & GEMM_F32_FLAG_TILE224) return tma ? 224 : 256;
   if (g.flags & GEMM_F32_FLAG_TILE256) return 256;
   if (split_tail) return g.M <= 64 ? 64 : (g.M <= 128 ? 128 : 256);
   const long tn = ceil_div(g.N, width);
   long best_cost = -1;
   int best = 256;
-  const int tms[3] = {256, 128, 64};
-  const long wide_pct[3] = {100, 81, 56}, narrow_pct[3] = {100, 96, 51};
+  const int tms[4] = {256, 224, 128, 64};
+  const long wide_pct[4] = {100, 98, 81, 56}, narrow_pct[4] = {100, 98, 96, 51};
   const long* const eff_pct = width == kTN ? wide_pct : narrow_pct;
-  for (int i = 0; i < 3; ++i) {
+  for (int i = 0; i < 4; ++i) {
+    if (tms[i] == 224 && !tma) continue;
     const long tiles = tn * ceil_div(g.M, tms[i]);
     const long rounds = (tiles + g.num_sms - 1) / g.num_sms;
     const long cost = rounds * tms[i] * 100 / eff_pct[i];
@@ -847,8 +894,8 @@ int choose_tm(const GemmArgs& g, bool split_tail, int width) {
 constexpr int kOneWaveMaxK = 2048;
 
 int one_wave_height(const GemmArgs& g, int tn) {
-  if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
-                 GEMM_F32_FLAG_ONE_TILE_PER_CTA))
+  if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE224 |
+                 GEMM_F32_FLAG_TILE256 | GEMM_F32_FLAG_ONE_TILE_PER_CTA))
     return 0;
   if (g.K > kOneWaveMaxK) return 0;
   const long tiles_n = ceil_div(g.N, tn);
@@ -861,6 +908,10 @@ int one_wave_height(const GemmArgs& g, int tn) {
 }
 
 }  // namespace
+
+// Least K iterations per CTA in a split tail that follows at least one full
+// wave of whole tiles.
+constexpr int kMinSplitItersMultiWave = 64;
 
 // Where a launch's split-tail scratch comes from: the library's workspace
 // for the stream (allocated on first use), or, for gemm_f32_noalloc, a
@@ -906,13 +957,14 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, const TailScratch& scratch, cud
   size_t ws_bytes = 0;
   const int one_wave_tm = one_wave_height(g, tn);
   if (!one_wave_tm && !(g.flags & (GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_NO_SPLIT_K))) {
-    tm = choose_tm(g, true, tn);
+    tm = choose_tm(g, true, tn, tma_ok);
     bk = bk_for(nprod, tm, tma_ok);
     p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
     const long tiles = static_cast<long>(p.tiles_m) * p.tiles_n;
     if (tiles <= 0x7fffffffL)
-      ws_bytes = plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * tn * sizeof(float));
+      ws_bytes = plan_split_tail(p, tiles, g.num_sms, static_cast<size_t>(tm) * tn * sizeof(float),
+                                 tiles >= g.num_sms ? kMinSplitItersMultiWave : kMinSplitIters);
   }
   void* ws = nullptr;
   if (ws_bytes) {
@@ -924,7 +976,7 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, const TailScratch& scratch, cud
     }
   }
   if (!ws) {
-    tm = one_wave_tm ? one_wave_tm : choose_tm(g, false, tn);
+    tm = one_wave_tm ? one_wave_tm : choose_tm(g, false, tn, tma_ok);
     bk = bk_for(nprod, tm, tma_ok);
     p.k_iters = ceil_div(g.K, bk);
     p.tiles_m = ceil_div(g.M, tm);
@@ -1012,7 +1064,7 @@ int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches
   // the TMA path: with per-thread loads the single-CTA kernel is faster
   // (1001 x 513 x 777: 31.6 against 55 us).
   const unsigned no_pair = GEMM_F32_FLAG_SINGLE_CTA | GEMM_F32_FLAG_TILE64 |
-                           GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
+                           GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE224 | GEMM_F32_FLAG_TILE256 |
                            GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_FORCE_STAGED;
   if (nprod == 1 && !(g.flags & no_pair) && tma_addressable(g) && g.M >= 256 && g.N >= 256 &&
       !one_wave_height(g, kTN))

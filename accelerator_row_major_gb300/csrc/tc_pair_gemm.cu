@@ -311,6 +311,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const bool trans_a = GEN && gp.trans_a, trans_b = GEN && gp.trans_b;
   using Cfg = PairCfg<BK, NPROD>;
   constexpr int S = Cfg::STAGES;
+  // extents (elements) of the arrays indexed by hand, for the checked build
+  [[maybe_unused]] const size_t a_extent =
+      trans_a ? stored_extent(p.K, p.M, lda) : stored_extent(p.M, p.K, lda);
+  [[maybe_unused]] const size_t b_extent =
+      trans_b ? stored_extent(p.N, p.K, ldb) : stored_extent(p.K, p.N, ldb);
+  [[maybe_unused]] const size_t c_extent = stored_extent(p.M, p.N, ldc);
+  [[maybe_unused]] const size_t work_extent =
+      static_cast<size_t>(p.tiles_m * p.tiles_n - p.dp_tiles) * p.max_seg * 2 * (kPairTile * kHalf);
   extern __shared__ uint8_t smem_dyn[];
   const uint32_t dyn0 = smem_addr(smem_dyn);
   const uint32_t base = (dyn0 + 1023u) & ~1023u;
@@ -498,7 +506,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_ld_32cols(t_acc + chunk * 32, v);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) mine[(chunk * 32 + j) * kHalf] = __uint_as_float(v[j]);
+          for (int j = 0; j < 32; ++j)
+            if (GEMM_IN_EXTENT(mine + (chunk * 32 + j) * kHalf - p.partials, work_extent, p.err,
+                               kSiteBoundsWork))
+              mine[(chunk * 32 + j) * kHalf] = __uint_as_float(v[j]);
         }
         __threadfence();
         epilogue_sync();
@@ -523,11 +534,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!scale) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (j < rows) dst[static_cast<size_t>(j) * ldc] = __uint_as_float(v[j]);
+                if (j < rows && GEMM_IN_EXTENT(dst + static_cast<size_t>(j) * ldc - p.C, c_extent,
+                                               p.err, kSiteBoundsC))
+                  dst[static_cast<size_t>(j) * ldc] = __uint_as_float(v[j]);
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j) {
-                if (j < rows) {
+                if (j < rows &&
+                    GEMM_IN_EXTENT(dst + static_cast<size_t>(j) * ldc - p.C, c_extent, p.err,
+                                   kSiteBoundsC)) {
                   float* d = dst + static_cast<size_t>(j) * ldc;
                   *d = pair_scaled_c(__uint_as_float(v[j]), d, gp.alpha, gp.beta);
                 }
@@ -607,7 +622,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int gm = m0 + r, gk = k0 + k;
               const size_t at = trans_a ? static_cast<size_t>(gk) * lda + gm
                                           : static_cast<size_t>(gm) * lda + gk;
-              av[j] = (gm < p.M && gk < p.K) ? __float_as_uint(__ldg(p.A + at)) : 0u;
+              av[j] = (gm < p.M && gk < p.K &&
+                       GEMM_IN_EXTENT(at, a_extent, p.err, kSiteBoundsA))
+                          ? __float_as_uint(__ldg(p.A + at))
+                          : 0u;
             }
             if (c0 == 0) {
 #pragma unroll
@@ -615,7 +633,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int gk = k0 + kh0 + k;
                 const size_t bt_at = trans_b ? static_cast<size_t>(gn) * ldb + gk
                                                : static_cast<size_t>(gk) * ldb + gn;
-                bv[k] = (gn < p.N && gk < p.K) ? __float_as_uint(__ldg(p.B + bt_at)) : 0u;
+                bv[k] = (gn < p.N && gk < p.K &&
+                         GEMM_IN_EXTENT(bt_at, b_extent, p.err, kSiteBoundsB))
+                            ? __float_as_uint(__ldg(p.B + bt_at))
+                            : 0u;
               }
             }
 #pragma unroll
@@ -680,7 +701,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < kBatch; ++i) {
             const int f = base + threadIdx.x + i * kThreads;
-            x[i] = f < kVec ? __ldcg(src + f) : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[i] = f < kVec && GEMM_IN_EXTENT(
+                                   4 * (src + f - reinterpret_cast<const float4*>(p.partials)) + 3,
+                                   work_extent, p.err, kSiteBoundsWork)
+                       ? __ldcg(src + f)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
           for (int i = 0; i < kBatch; ++i) {
@@ -702,7 +727,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq)
               if (n + qq < p.N)
-                dst[qq] = scale ? pair_scaled_c(vals[qq], dst + qq, gp.alpha, gp.beta) : vals[qq];
+                if (GEMM_IN_EXTENT(dst + qq - p.C, c_extent, p.err, kSiteBoundsC))
+                  dst[qq] = scale ? pair_scaled_c(vals[qq], dst + qq, gp.alpha, gp.beta) : vals[qq];
           }
         }
       }
@@ -764,8 +790,8 @@ int launch_pair_one(const GemmArgs& g, const PairParams& p, const PairGeneral& g
 bool tc_pair_suits(const GemmArgs& g) {
   if (g.flags & GEMM_F32_FLAG_SINGLE_CTA) return false;
   if (g.flags & GEMM_F32_FLAG_CTA_PAIR) return true;
-  if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE256 |
-                 GEMM_F32_FLAG_ONE_TILE_PER_CTA))
+  if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE224 |
+                 GEMM_F32_FLAG_TILE256 | GEMM_F32_FLAG_ONE_TILE_PER_CTA))
     return false;
   const long tiles = static_cast<long>((g.M + kPairTile - 1) / kPairTile) *
                      ((g.N + kPairTile - 1) / kPairTile);

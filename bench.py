@@ -42,10 +42,9 @@ import workloads  # noqa: E402
 
 METRIC = "FP32 GEMM TFLOPS (2MNK/t) at 1 GB300 and % of 3xTF32 / FFMA roofline"
 L2_BYTES = 129 * 1024 * 1024
-# nominal dense ratios (tf32 : bf16 tensor rate) used to scale the measured bf16 peak
+# nominal dense ratio (tf32 : bf16 tensor rate): scales the measured bf16
+# cuBLAS peak into the secondary tensor roof the line also reports
 TF32_PER_BF16 = 1.1 / 2.25
-# CUDA-core fp32: 128 lanes x 2 FLOP per SM per clock
-FFMA_FLOP_PER_SM_CLK = 256
 MODE_PRODUCTS = {"tc3x": 3, "tc1x": 1, "ffma": 1}
 
 
@@ -62,6 +61,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-sub-modes", action="store_true",
+                    help="leave out the ffma and tc1x records timed beside the headline mode")
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the one-line benchmark: every problem of workloads.py in every "
                          "mode, warm and cold L2, mean and median, and the pages' statistic (one "
@@ -128,30 +129,36 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 50 ms while active."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while active,
+    each sample with its timestamp, so that the samples of a window (the
+    timed steps) can be told from the rest (warm-up)."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index: int, enabled: bool = True):
+    def __init__(self, index: int, enabled: bool = True, period_ms: int = 20):
         self.index = index
         self.proc = None
         self.enabled = enabled
+        self.period_ms = period_ms
+        self.lines = []
 
     def __enter__(self):
         if self.enabled:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                     "--format=csv,noheader,nounits", "-lms", "50"],
+                     "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                     stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             except OSError:
                 self.proc = None
+            time.sleep(0.3)          # the first sample is out before the work starts
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
+            time.sleep(2.0 * self.period_ms / 1e3)
             self.proc.terminate()
             try:
                 out, _ = self.proc.communicate(timeout=5)
@@ -161,22 +168,41 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
-    def summary(self):
+    def samples(self):
+        """[(unix time, sm MHz, max sm MHz, [reason flags])]"""
+        import datetime
         rows = []
-        for line in getattr(self, "lines", []):
+        for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                when = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((when, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
+        return rows
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and throttle reasons over the samples taken in
+        [t0, t1] (host wall-clock seconds); over every sample when that window
+        holds fewer than 3 (a timed region shorter than a few sample periods),
+        which the record says."""
+        rows = self.samples()
         if not rows:
             return None
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, flags in rows for i, v in enumerate(flags) if v == "Active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        window = "timed steps"
+        if t0 is not None:
+            inside = [r for r in rows if t0 <= r[0] <= t1]
+            if len(inside) < 3:
+                window = "warm-up and timed steps (%d samples inside the timed steps)" % len(inside)
+                inside = [r for r in rows if r[0] <= t1]
+            rows = inside or rows
+        reasons = sorted({self.REASONS[i] for _, _, _, flags in rows for i, v in enumerate(flags)
+                          if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(rows), "window": window,
+                "period_ms": self.period_ms}
 
 
 # the sources each kernel's device code comes from: its own file and the
@@ -329,8 +355,112 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------- GPU timing
+def roofline(kernel, mode, flop, work_bytes, t_kernel, rates, clocks, peaks, peak_src):
+    """The binding roof of one launch of `kernel`.  Compute roofs are the
+    probed per-SM rate of the unit doing the work (gemm_f32_unit_rates: FLOP
+    per SM per clock) x SMs x the median SM clock sampled while the steps ran;
+    the memory roof is the measured copy bandwidth."""
+    sms = rates["num_sms"]
+    mhz = clocks["sm_mhz"] if clocks else rates["sm_mhz"]
+    clock_src = "median SM clock sampled over the %s" % clocks["window"] if clocks else \
+        "SM clock during the unit probe (no nvidia-smi samples)"
+    if mode == "ffma":
+        peak = rates["ffma_flop_per_clk_sm"] * sms * mhz * 1e6 / 1e12
+        roof = {"bound": "alu", "achieved": flop / t_kernel / 1e12, "peak": peak, "unit": "TFLOP/s",
+                "peak_source": "probed fma.rn.f32x2 rate %.1f FLOP/clk/SM x %d SMs x %.0f MHz (%s)"
+                               % (rates["ffma_flop_per_clk_sm"], sms, mhz, clock_src)}
+    else:
+        nprod = MODE_PRODUCTS[mode]
+        per_clk = rates["tf32_pair_flop_per_clk_sm"] if kernel == "tc_pair_kernel" \
+            else rates["tf32_flop_per_clk_sm"]
+        peak = per_clk * sms * mhz * 1e6 / 1e12
+        hbm = peaks.get("hbm_gbs")
+        # the binding roof: the larger of the two lower bounds on the time
+        if hbm and work_bytes / (hbm * 1e9) > nprod * flop / (peak * 1e12):
+            roof = {"bound": "hbm", "achieved": work_bytes / t_kernel / 1e9, "peak": hbm,
+                    "unit": "GB/s",
+                    "peak_source": "%s copy bandwidth; achieved = algorithmic bytes "
+                                   "4(MK + KN + MN) per launch / time" % peak_src}
+        else:
+            roof = {"bound": "tensor", "achieved": nprod * flop / t_kernel / 1e12, "peak": peak,
+                    "unit": "TFLOP/s",
+                    "peak_source": "probed tcgen05 kind::tf32 rate %.0f FLOP/clk/SM (%s) x %d SMs x "
+                                   "%.0f MHz (%s); achieved counts the %d tf32 products per fp32 product"
+                                   % (per_clk, "SM pairs" if kernel == "tc_pair_kernel" else "one SM",
+                                      sms, mhz, clock_src, nprod)}
+            bf16 = peaks["bf16_tflops"] * TF32_PER_BF16
+            roof["secondary"] = {"peak": bf16, "frac": roof["achieved"] / bf16,
+                                 "peak_source": "%s bf16 cuBLAS burst x nominal tf32/bf16 ratio "
+                                                "1.1/2.25" % peak_src}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["frac_of"] = "measured"
+    return roof
+
+
+def time_product(g, A, B, C, M, N, K, mode, flags, stream, steps, warmup, flush, scratch, dist_mod,
+                 device, clocks_enabled, local_rank):
+    """W warm-up calls, then exactly `steps` timed calls (CUDA events on the
+    launching stream, a barrier and a synchronise on both sides), with
+    nvidia-smi sampling from before the warm-up to after the timed steps.
+    Returns (max-over-ranks ms per step, kernels per call, kernel name,
+    clock summary of the timed window)."""
+    import torch
+
+    def step():
+        rc = g.gemm_f32_ex(A, B, C, M, N, K, mode, flags, stream)
+        if rc != 0:
+            raise g.GemmError(rc, "gemm_f32_ex")
+
+    events = []
+    with ClockSampler(local_rank, enabled=clocks_enabled) as clocks:
+        torch.cuda.synchronize(device)
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, warmup)):
+                step()
+        launches_per_step = g.gemm_f32_last_launches()
+        kernel = g.gemm_f32_last_kernel()
+        rc, site = g.gemm_f32_status(stream)
+        if rc != 0:
+            raise SystemExit("device error word %d after warm-up" % site)
+        barrier(dist_mod, device)
+        torch.cuda.synchronize(device)
+        t_start = time.time()
+        with torch.cuda.stream(stream):
+            if flush:
+                for _ in range(steps):
+                    scratch.zero_()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    step()
+                    e1.record(stream)
+                    events.append((e0, e1))
+            else:
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(steps):
+                    step()
+                e1.record(stream)
+                events.append((e0, e1))
+        torch.cuda.synchronize(device)
+        t_end = time.time()
+        barrier(dist_mod, device)
+    device_ms = sum(a.elapsed_time(b) for a, b in events)
+    rc, site = g.gemm_f32_status(stream)
+    if rc != 0:
+        raise SystemExit("device error word %d in the timed region" % site)
+    ms_per_step = max_over_ranks(device_ms / steps, dist_mod, device)
+    return ms_per_step, launches_per_step, kernel, clocks.summary(t_start, t_end)
+
+
+# modes reported beside the headline one, on the same problem, when the
+# default problem is benchmarked (each with its own roof and clocks)
+SUB_MODES = ("ffma", "tc1x")
+
+
 def run_ours(args):
-    import numpy as np
+    import numpy as np  # noqa: F401
     import torch
 
     rank, world, local_rank = dist_env()
@@ -355,52 +485,27 @@ def run_ours(args):
     work_bytes = workloads.algorithmic_bytes(M, N, K)
     flush = work_bytes < 2 * L2_BYTES
     scratch = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device) if flush else None
+    rates = g.gemm_f32_unit_rates()        # per-SM unit rates: the compute roofs
 
-    def step():
-        rc = g.gemm_f32_ex(A, B, C, M, N, K, args.mode, args.flags, stream)
-        if rc != 0:
-            raise g.GemmError(rc, "gemm_f32_ex")
-
-    torch.cuda.synchronize(device)
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            step()
-    launches_per_step = g.gemm_f32_last_launches()
-    kernel = g.gemm_f32_last_kernel()
-    rc, site = g.gemm_f32_status(stream)
-    if rc != 0:
-        raise SystemExit("device error word %d after warm-up" % site)
-
-    events = []
-    with ClockSampler(local_rank, enabled=not args.no_clocks) as clocks:
-        barrier(dist_mod, device)
-        torch.cuda.synchronize(device)
-        with torch.cuda.stream(stream):
-            if flush:
-                for _ in range(args.steps):
-                    scratch.zero_()
-                    e0 = torch.cuda.Event(enable_timing=True)
-                    e1 = torch.cuda.Event(enable_timing=True)
-                    e0.record(stream)
-                    step()
-                    e1.record(stream)
-                    events.append((e0, e1))
-            else:
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(args.steps):
-                    step()
-                e1.record(stream)
-                events.append((e0, e1))
-        torch.cuda.synchronize(device)
-        barrier(dist_mod, device)
-    device_ms = sum(a.elapsed_time(b) for a, b in events)
-    rc, site = g.gemm_f32_status(stream)
-    if rc != 0:
-        raise SystemExit("device error word %d in the timed region" % site)
-    ms_per_step = max_over_ranks(device_ms / args.steps, dist_mod, device)
+    ms_per_step, launches_per_step, kernel, clocks = time_product(
+        g, A, B, C, M, N, K, args.mode, args.flags, stream, args.steps, args.warmup, flush, scratch,
+        dist_mod, device, not args.no_clocks, local_rank)
     value = whole_job_tflops(flop, args.steps, world, ms_per_step * args.steps / 1e3)
+
+    # ---- the other modes on the same problem, each timed the same way
+    subs = {}
+    if not args.no_sub_modes and args.flags == 0:
+        for mode in SUB_MODES:
+            if mode == args.mode:
+                continue
+            ms, launches, kern, clk = time_product(
+                g, A, B, C, M, N, K, mode, 0, stream, args.steps, args.warmup, flush, scratch,
+                dist_mod, device, not args.no_clocks, local_rank)
+            subs[mode] = {"value": whole_job_tflops(flop, args.steps, world, ms * args.steps / 1e3),
+                          "unit": "TFLOPS", "ms_per_step": ms, "steps": args.steps,
+                          "warmup": args.warmup, "kernel": kern,
+                          "gpu_launches": launches * args.steps, "clocks": clk,
+                          "roofline": None, "_t": ms / 1e3}
 
     # ---- end to end through the C-ABI call with host buffers
     e2e = None
@@ -459,31 +564,15 @@ def run_ours(args):
         return 0
 
     peaks, peak_src = measured_peaks()
-    t_kernel = ms_per_step / 1e3  # one launch per step
-    if args.mode == "ffma":
-        peak = FFMA_FLOP_PER_SM_CLK * torch.cuda.get_device_properties(device).multi_processor_count \
-            * peaks.get("sm_max_mhz", 2070.0) * 1e6 / 1e12
-        roof = {"bound": "alu", "achieved": flop / t_kernel / 1e12, "peak": peak, "unit": "TFLOP/s",
-                "peak_source": "fp32 lanes x SMs x max SM clock (%s clock)" % peak_src}
-    else:
-        peak = peaks["bf16_tflops"] * TF32_PER_BF16
-        nprod = MODE_PRODUCTS[args.mode]
-        hbm = peaks.get("hbm_gbs")
-        # the binding roof: the larger of the two lower bounds on the time
-        if hbm and work_bytes / (hbm * 1e9) > nprod * flop / (peak * 1e12):
-            roof = {"bound": "hbm", "achieved": work_bytes / t_kernel / 1e9, "peak": hbm,
-                    "unit": "GB/s",
-                    "peak_source": "%s copy bandwidth; achieved = algorithmic bytes "
-                                   "4(MK + KN + MN) per launch / time" % peak_src}
-        else:
-            roof = {"bound": "tensor", "achieved": nprod * flop / t_kernel / 1e12, "peak": peak,
-                    "unit": "TFLOP/s",
-                    "peak_source": "%s bf16 burst x nominal tf32/bf16 ratio; achieved counts the %d "
-                                   "tf32 products per fp32 product" % (peak_src, nprod)}
-    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof = roofline(kernel, args.mode, flop, work_bytes, ms_per_step / 1e3, rates, clocks, peaks,
+                    peak_src)   # one launch per step
     roof["kernel"] = kernel
     roof["traffic"] = recorded_traffic(kernel, args.config, args.mode)
     roof["algorithmic_bytes"] = work_bytes
+    for mode, sub in subs.items():
+        sub["roofline"] = roofline(sub["kernel"], mode, flop, work_bytes, sub.pop("_t"), rates,
+                                   sub["clocks"], peaks, peak_src)
+        sub["roofline"]["traffic"] = recorded_traffic(sub["kernel"], args.config, mode)
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -493,12 +582,14 @@ def run_ours(args):
                        "flags": args.flags,
                        "l2": "flushed between steps" if flush else "inputs larger than L2",
                        "parallelism": "replicas x%d" % world},
-            "roofline": roof, "gpu_launches": launches_per_step * args.steps}
+            "roofline": roof, "gpu_launches": launches_per_step * args.steps,
+            "unit_rates": rates}
     if e2e is not None:
         line["e2e"] = e2e
-    cs = clocks.summary()
-    if cs is not None:
-        line["clocks"] = cs
+    if clocks is not None:
+        line["clocks"] = clocks
+    for mode, sub in subs.items():
+        line[mode] = sub
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = oracle_sample(A_h, B_h, args.cpu_seconds)[0]
     print(json.dumps(line), flush=True)

@@ -87,9 +87,11 @@ enum gemm_f32_mode {
                                             per-thread masked loads even where
                                             the tensor-memory-accelerator path
                                             is possible                       */
-#define GEMM_F32_FLAG_TILE64 0x10u       /* tensor modes: output tiles of 64   */
-#define GEMM_F32_FLAG_TILE128 0x20u      /*   ... 128 or 256 rows of C (by 128 */
-#define GEMM_F32_FLAG_TILE256 0x40u      /*   columns); default: chosen by size */
+#define GEMM_F32_FLAG_TILE64 0x10u       /* tensor modes: output tiles of 64,  */
+#define GEMM_F32_FLAG_TILE128 0x20u      /*   128, 224 or 256 rows of C (by 128 */
+#define GEMM_F32_FLAG_TILE224 0x80u      /*   columns; 224 with TMA-readable    */
+#define GEMM_F32_FLAG_TILE256 0x40u      /*   operands only, else 256);         */
+                                         /*   default: chosen by size           */
 #define GEMM_F32_FLAG_ONE_TILE_PER_CTA 0x100u /* launch one CTA per output
                                             tile instead of the persistent grid */
 #define GEMM_F32_FLAG_NO_SPLIT_K 0x200u  /* never split the last wave along K
@@ -302,7 +304,14 @@ typedef struct {
 
 int gemm_f32_unit_rates(gemm_f32_unit_rates_t* rates);
 
-/* Static version string, e.g. "gemm_f32 1.0 sm_103a". */
+/* Static version string, e.g. "gemm_f32 1.0 sm_103a"; the debug library
+ * built with -DGEMM_BOUNDS_CHECK (libgemm_f32_checked.so) appends
+ * " bounds-checked".  In that build every hand-indexed global load and store
+ * is checked against its array's extent: an index outside records site
+ * 16 (A), 17 (B), 18 (C), 19 (split-tail partials) or 20 (operand copies)
+ * in the error word that gemm_f32_status() reads, and the access is
+ * skipped, as out-of-range elements are in "Lesson 10: shared-memory tiled
+ * GEMM" (hpc.payai.win, section 3). */
 const char* gemm_f32_version(void);
 
 #ifdef __cplusplus

@@ -124,3 +124,16 @@ def test_plain_form_equals_gemm_f32_ex():
         g.check(g.gemm_f32_general(0, 0, 700, 500, 300, 1.0, a, 300, b, 500, 0.0, c2, 500, mode))
         torch.cuda.synchronize()
         assert torch.equal(c1.view(torch.int32), c2.view(torch.int32)), mode
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (1, 1)])
+@pytest.mark.parametrize("shape", [(3000, 60, 700), (60, 3000, 700), (5000, 64, 2048)])
+def test_general_ffma_skinny_tiles(shape, ta, tb):
+    """FFMA's tiles for N <= 64 (256 x 64) and M <= 64 (64 x 256) in the
+    general form: strides, stored transposes, alpha / beta, split tails."""
+    M, N, K = shape
+    A, B, C0 = case(50 + M + ta, M, N, K, ta, tb)
+    Co, absC = oracle.gemm_general(A, B, C0, M, N, K, alpha=-1.25, beta=0.5, trans_a=ta, trans_b=tb)
+    C = run_general(A, B, C0, M, N, K, -1.25, 0.5, ta, tb, "ffma")
+    assert lib().gemm_f32_last_kernel() == "ffma_gemm_kernel"
+    assert_close(C[:M, :N], Co[:M, :N], absC, TOL["ffma"], "ffma skinny %s %d%d" % (shape, ta, tb))

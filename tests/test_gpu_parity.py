@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
 
 MODES = ["tc3x", "ffma", "tc1x"]
 FLAG_STAGED = 0x1
-FLAG_TILE = {64: 0x10, 128: 0x20, 256: 0x40}
+FLAG_TILE = {64: 0x10, 128: 0x20, 224: 0x80, 256: 0x40}
 FLAG_ONE_TILE = 0x100
 FLAG_NO_SPLIT = 0x200
 FLAG_PAIR = 0x400
@@ -420,3 +420,63 @@ def test_split_tail_repeats_with_other_work_between(mode, shape):
     vals, absv = oracle.gemm_entries(A, B, rows, cols)
     assert_close(first[rows, cols][None, :], vals[None, :], absv[None, :], TOL[mode],
                  "split repeats %s/%s" % (shape, mode))
+
+
+FFMA_SKINNY = [(1000, 300, 64), (517, 129, 60), (64, 4096, 3000), (33, 1000, 5000),
+               (20000, 1024, 64), (64, 20000, 512), (65, 777, 63), (300, 2048, 1)]
+
+
+@pytest.mark.parametrize("shape", FFMA_SKINNY)
+def test_ffma_skinny_tiles(shape):
+    """FFMA block tiles of 256 x 64 (N <= 64) and 64 x 256 (M <= 64), two
+    CTAs per SM: ragged edges, split tails (long K, few tiles) and whole
+    tiles, deterministic, against the oracle on every element."""
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "normal", 880 + M + N)
+    Co, absAB = oracle_full(A, B)
+    C, outs = run_abi(A, B, "ffma", FLAG_SINGLE, repeats=2)
+    assert lib().gemm_f32_last_kernel() == "ffma_gemm_kernel"
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert_close(C, Co, absAB, TOL["ffma"], "ffma skinny %s" % (shape,))
+    for flags in (FLAG_NO_SPLIT, FLAG_ONE_TILE):
+        C, _ = run_abi(A, B, "ffma", flags)
+        assert_close(C, Co, absAB, TOL["ffma"], "ffma skinny %s/%#x" % (shape, flags))
+    C, _ = run_abi(A, B, "ffma", FLAG_SINGLE, offset_a=1, offset_b=3)
+    assert_close(C, Co, absAB, TOL["ffma"], "ffma skinny %s/misaligned" % (shape,))
+
+
+def test_ffma_skinny_integers_exact():
+    for (M, K, N) in ((700, 512, 64), (64, 512, 900)):
+        A, B = workloads.make_inputs(M, K, N, "int8", 5 + M)
+        Co, _ = oracle_full(A, B)
+        C, _ = run_abi(A, B, "ffma", FLAG_SINGLE)
+        assert_bit_exact(C, Co, "ffma skinny int %dx%dx%d" % (M, K, N))
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+@pytest.mark.parametrize("shape,flags", [
+    ((1024, 512, 1024), FLAG_TILE[224]),      # 5 tile rows, the last one 128 rows
+    ((1000, 300, 64), FLAG_TILE[224]),        # narrow tiles
+    ((2000, 8192, 64), FLAG_TILE[224]),       # split tail: partials of 224 x 64 (odd float4 count per thread)
+    ((2000, 8192, 300), FLAG_TILE[224]),      # split tail, 128-column tiles
+    ((60000, 1024, 100), 0),                  # chosen by the wave model: 268 tiles, two waves
+    ((60000, 512, 64), 0),                    # chosen, narrow
+])
+def test_tiles_of_224_rows(mode, shape, flags):
+    """224-row tiles (TMA path): ragged last tile rows, split tails and the
+    heights the wave model picks, against the oracle on every element."""
+    M, K, N = shape
+    A, B = workloads.make_inputs(M, K, N, "normal", 224 + M + N)
+    Co, absAB = oracle_full(A, B)
+    C, outs = run_abi(A, B, mode, flags, repeats=2)
+    assert lib().gemm_f32_last_kernel() == "tc_gemm_kernel"
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    assert_close(C, Co, absAB, TOL[mode], "224 rows %s/%s/%#x" % (shape, mode, flags))
+
+
+@pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
+def test_tiles_of_224_rows_integers_exact(mode):
+    A, B = workloads.make_inputs(1000, 512, 200, "int8", 224)
+    Co, _ = oracle_full(A, B)
+    C, _ = run_abi(A, B, mode, FLAG_TILE[224])
+    assert_bit_exact(C, Co, "224 rows int/%s" % mode)
