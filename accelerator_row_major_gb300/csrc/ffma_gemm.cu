@@ -1,10 +1,10 @@
 // CUDA-core FP32 GEMM (FFMA) for sm_103a: persistent CTAs, 8 x 16 outputs
 // per thread, a 4-stage cp.async shared-memory ring, and the paired fp32
 // fused multiply-add (fma.rn.f32x2: two FMAs per lane per instruction, each
-// rounded once like fmaf).  Block tiles: 128 x 256 (256 threads, one CTA per
-// SM); 256 x 64 for N <= 64 and 64 x 256 for M <= 64 (128 threads, two CTAs
-// per SM), so that skinny products spend no multiply-adds on rows or
-// columns beyond the matrix.
+// rounded once like fmaf).  Block tiles of 256 threads, one CTA per SM:
+// 128 x 256, and 512 x 64 for N <= 64 and 64 x 512 for M <= 64, so that
+// skinny products spend no multiply-adds on rows or columns beyond the
+// matrix.
 //
 // Computes C[i][j] = sum_k A[i][k] * B[k][j] (row-major) in fp32 fused
 // multiply-adds, k ascending per output.  The structure follows the pages'
@@ -46,14 +46,14 @@ using namespace gemm_f32_dev;
 namespace {
 
 constexpr int kBK = 16;
-constexpr int kStages = 4;
 constexpr int kAPitch = kBK + 4;               // floats per A row in shared memory
 constexpr int kRasterGroup = 8;
 
 // A block tile of BM x BN outputs, 8 x 16 per thread.
-template <int BM_, int BN_>
+template <int BM_, int BN_, int STAGES_ = 4>
 struct FfmaTile {
   static constexpr int BM = BM_, BN = BN_;
+  static constexpr int STAGES = STAGES_;                  // cp.async ring depth
   static constexpr int TY = BM / 8, TX = BN / 16;       // threads along rows / columns
   static constexpr int THREADS = TX * TY;
   static constexpr int LX = TX < 8 ? TX : 8;              // lanes of a warp along columns
@@ -62,12 +62,18 @@ struct FfmaTile {
   static constexpr int CTAS_PER_SM = 256 / THREADS;       // 8 warps per SM
   static constexpr int A_STAGE = BM * kAPitch;            // floats
   static constexpr int B_STAGE = kBK * BN;                // floats
-  static constexpr int SMEM = kStages * (A_STAGE + B_STAGE) * 4;
+  static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) * 4;
   static_assert(THREADS % 32 == 0 && BM * 4 % THREADS == 0 && BN * 4 % THREADS == 0, "tile");
 };
+// The skinny tiles keep 256 threads in one CTA per SM: measured on GB300
+// (per-CTA timestamps), two 128-thread CTAs sharing an SM do not share it
+// evenly -- one finishes its (equal) work in 57 % of the time of the other,
+// which then runs on 4 warps, too few to keep the FMA pipe busy (64 x 4096
+// x 65536 with 64 x 256 tiles: CTAs ending at 360-370 us and 640-647 us, an
+// average of 6.3 resident warps out of 8).
 using TileWide = FfmaTile<128, 256>;     // default
-using TileTall = FfmaTile<256, 64>;      // N <= 64
-using TileShort = FfmaTile<64, 256>;     // M <= 64
+using TileTall = FfmaTile<512, 64>;      // N <= 64
+using TileShort = FfmaTile<64, 512>;     // M <= 64
 constexpr int kMaxPending = 8;               // split tiles one CTA may have to reduce
 // An FFMA K iteration costs ~6x a tensor-core one, so splitting the tail pays
 // off at far fewer iterations per CTA (measured on GB300: 2.5x on 1024 x 512 x
@@ -221,6 +227,7 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
   __shared__ WorkItem pending[kMaxPending];   // split tiles this CTA must reduce
   __shared__ int pending_count;
   float* const As = smem_f;                          // [stage][BM][kAPitch]
+  constexpr int kStages = T::STAGES;
   float* const Bs = smem_f + kStages * T::A_STAGE;   // [stage][16][BN]
   const uint32_t as_addr = smem_addr(As), bs_addr = smem_addr(Bs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -405,9 +412,9 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
 constexpr int kMaxDevices = 64;
 
 // Configures the kernel once per device (its dynamic shared memory, and all
-// of the unified L1 / shared memory as shared memory: two CTAs of the
-// 128-thread tiles, 96 KB each, fit on an SM only with it) and returns how
-// many of its CTAs an SM holds (0 on failure).
+// of the unified L1 / shared memory as shared memory: the 512 x 64 tile's
+// four stages take 176 KB) and returns how many of its CTAs an SM holds (0 on
+// failure), which the persistent grid is planned with.
 template <class T, bool VEC, bool GEN>
 int resident_ctas(int device) {
   static std::atomic<int> per_sm[kMaxDevices];   // 0: not configured yet

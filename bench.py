@@ -513,7 +513,7 @@ def run_ours(args):
         A_pin = torch.from_numpy(A_h).pin_memory()
         B_pin = torch.from_numpy(B_h).pin_memory()
         C_pin = torch.empty((M, N), dtype=torch.float32).pin_memory()
-        e2e_steps = max(3, args.steps // 4)
+        e2e_steps = max(8, args.steps // 2)   # enough calls that the first copy-in is amortised
 
         def e2e_call():
             # copies A and B in, computes, copies C out (gemm_f32_host)
