@@ -35,6 +35,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdint>
+#include <cstring>
 
 #include "../../include/gemm_f32.h"
 #include "device_common.cuh"
@@ -53,17 +54,28 @@ constexpr int kRasterGroup = 8;
 template <int BM_, int BN_, int STAGES_ = 4>
 struct FfmaTile {
   static constexpr int BM = BM_, BN = BN_;
-  static constexpr int STAGES = STAGES_;                  // cp.async ring depth
+  static constexpr int STAGES = STAGES_;                  // shared-memory ring depth
   static constexpr int TY = BM / 8, TX = BN / 16;       // threads along rows / columns
   static constexpr int THREADS = TX * TY;
   static constexpr int LX = TX < 8 ? TX : 8;              // lanes of a warp along columns
   static constexpr int WX = TX / LX;                      // warps along columns
   static constexpr int CG = BN / 4;                       // column-group stride
   static constexpr int CTAS_PER_SM = 256 / THREADS;       // 8 warps per SM
-  static constexpr int A_STAGE = BM * kAPitch;            // floats
+  static constexpr int A_STAGE = BM * kAPitch;            // floats, per-thread copies
   static constexpr int B_STAGE = kBK * BN;                // floats
   static constexpr int SMEM = STAGES * (A_STAGE + B_STAGE) * 4;
+  // TMA loads: A stages dense (BM rows of 16 floats, 64-byte swizzle), in
+  // boxes of at most 256 rows; B stages of 16 rows, in boxes of at most 256
+  // columns ([box][16][A_BOX... B_BOX]); 1024-byte aligned.
+  static constexpr int A_BOX = BM < 256 ? BM : 256;
+  static constexpr int B_BOX = BN < 256 ? BN : 256;
+  static constexpr int A_STAGE_TMA = BM * kBK;            // floats
+  static constexpr int STAGE_BYTES_TMA = (A_STAGE_TMA + B_STAGE) * 4;
+  static constexpr int SMEM_TMA = STAGES * STAGE_BYTES_TMA + 1024;
   static_assert(THREADS % 32 == 0 && BM * 4 % THREADS == 0 && BN * 4 % THREADS == 0, "tile");
+  // a thread's rows ty + TY i share one swizzle phase ((row >> 1) & 3)
+  static_assert(TY % 8 == 0 && BM % A_BOX == 0 && BN % B_BOX == 0, "TMA tile");
+  static_assert((A_STAGE_TMA * 4) % 1024 == 0 && STAGE_BYTES_TMA % 1024 == 0, "TMA alignment");
 };
 // The skinny tiles keep 256 threads in one CTA per SM: measured on GB300
 // (per-CTA timestamps), two 128-thread CTAs sharing an SM do not share it
@@ -92,6 +104,7 @@ struct FfmaParams {
   int max_seg;           // most CTAs sharing one tail tile
   float* partials;       // [tail tile][max_seg][BM][BN] fp32
   unsigned long long* counters;   // [tail tile]: generation and partials published
+  int drop_first_copy;   // testing only (TMA loads): CTA 0 never fills its first stage
   unsigned* err;
 };
 
@@ -127,11 +140,6 @@ __device__ __forceinline__ float2 unpair(uint64_t v) {
   return r;
 }
 
-__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
@@ -146,12 +154,10 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Copies K tile `kt` of the block's A panel and B panel into one stage.
-// VEC: K % 4 == 0, N % 4 == 0, untransposed operands with row strides a
-// multiple of 4 and 16-byte aligned A and B, so a 16-byte chunk is either
-// wholly inside the matrix or wholly outside.  Otherwise 4-byte copies, which
-// also read transposed storage.
-template <class T, bool VEC, bool GEN>
+// Copies K tile `kt` of the block's A panel and B panel into one stage with
+// 4-byte cp.async copies (any alignment, any stride, transposed storage);
+// out-of-range elements are zero-filled.
+template <class T, bool GEN>
 __device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGeneral& gp, int m0,
                                            int n0, int kt,
                                            uint32_t a_dst, uint32_t b_dst) {
@@ -170,21 +176,13 @@ __device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGenera
     const int r = c >> 2, kc = (c & 3) * 4;
     const int gm = m0 + r, gk = k0 + kc;
     const uint32_t dst = a_dst + (r * kAPitch + kc) * 4;
-    if (VEC) {
-      const bool in = gm < p.M && gk < p.K &&
-                      GEMM_IN_EXTENT(static_cast<size_t>(gm) * lda + gk + 3, a_extent, p.err,
-                                     kSiteBoundsA);
-      const float* src = in ? p.A + static_cast<size_t>(gm) * lda + gk : p.A;
-      cp_async_16(dst, src, in ? 16u : 0u);
-    } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const size_t at = trans_a ? static_cast<size_t>(gk + e) * lda + gm
-                                  : static_cast<size_t>(gm) * lda + gk + e;
-        const bool in = gm < p.M && gk + e < p.K &&
-                        GEMM_IN_EXTENT(at, a_extent, p.err, kSiteBoundsA);
-        cp_async_4(dst + 4 * e, in ? p.A + at : p.A, in ? 4u : 0u);
-      }
+    for (int e = 0; e < 4; ++e) {
+      const size_t at = trans_a ? static_cast<size_t>(gk + e) * lda + gm
+                                : static_cast<size_t>(gm) * lda + gk + e;
+      const bool in = gm < p.M && gk + e < p.K &&
+                      GEMM_IN_EXTENT(at, a_extent, p.err, kSiteBoundsA);
+      cp_async_4(dst + 4 * e, in ? p.A + at : p.A, in ? 4u : 0u);
     }
   }
   // B: 16 k x BN columns = 4 BN chunks; thread -> chunks tid + THREADS h
@@ -194,31 +192,63 @@ __device__ __forceinline__ void load_stage(const FfmaParams& p, const FfmaGenera
     const int k = c / (T::BN / 4), nc = (c % (T::BN / 4)) * 4;
     const int gk = k0 + k, gn = n0 + nc;
     const uint32_t dst = b_dst + (k * T::BN + nc) * 4;
-    if (VEC) {
-      const bool in = gk < p.K && gn < p.N &&
-                      GEMM_IN_EXTENT(static_cast<size_t>(gk) * ldb + gn + 3, b_extent, p.err,
-                                     kSiteBoundsB);
-      const float* src = in ? p.B + static_cast<size_t>(gk) * ldb + gn : p.B;
-      cp_async_16(dst, src, in ? 16u : 0u);
-    } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const size_t at = trans_b ? static_cast<size_t>(gn + e) * ldb + gk
-                                  : static_cast<size_t>(gk) * ldb + gn + e;
-        const bool in = gk < p.K && gn + e < p.N &&
-                        GEMM_IN_EXTENT(at, b_extent, p.err, kSiteBoundsB);
-        cp_async_4(dst + 4 * e, in ? p.B + at : p.B, in ? 4u : 0u);
+    for (int e = 0; e < 4; ++e) {
+      const size_t at = trans_b ? static_cast<size_t>(gn + e) * ldb + gk
+                                : static_cast<size_t>(gk) * ldb + gn + e;
+      const bool in = gk < p.K && gn + e < p.N &&
+                      GEMM_IN_EXTENT(at, b_extent, p.err, kSiteBoundsB);
+      cp_async_4(dst + 4 * e, in ? p.B + at : p.B, in ? 4u : 0u);
+    }
+  }
+}
+
+// One stage of the inner product: acc += A tile x B tile over its 16 k.
+// `a_at(i, kg)` gives the shared-memory float offset of the float4 of row
+// ty + TY i, k 4 kg .. 4 kg + 3; `b_at(k, g)` that of the float4 of row k,
+// columns CG g + 4 tx .. + 3.
+template <class T, class AAt, class BAt>
+__device__ __forceinline__ void stage_product(const float* as, const float* bs, AAt a_at, BAt b_at,
+                                              uint64_t (&acc)[8][8]) {
+#pragma unroll
+  for (int kg = 0; kg < kBK / 4; ++kg) {
+    float4 a4[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a4[i] = *reinterpret_cast<const float4*>(as + a_at(i, kg));
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint64_t b[8];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(bs + b_at(kg * 4 + kk, g));
+        b[2 * g] = v.x;
+        b[2 * g + 1] = v.y;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
+        const uint64_t aa = pair(a, a);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[i][q] = fma2(aa, b[q], acc[i][q]);
       }
     }
   }
 }
 
+// VEC: operands the tensor-memory accelerator can read (untransposed, row
+// strides a multiple of 4 floats, 16-byte aligned bases): one thread loads
+// each stage with TMA boxes, completion counted on the stage's mbarrier, and
+// every thread waits on it (bounded, as in the tensor-core kernels).
+// Otherwise every thread copies 4-byte elements with cp.async.
 // GEN: the general form (row strides, stored transposes, alpha / beta); a
 // separate instantiation, so that the plain product's code is unchanged.
 template <class T, bool VEC, bool GEN>
 __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
-    ffma_gemm_kernel(const FfmaParams p, const FfmaGeneral gp) {
+    ffma_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB, const FfmaParams p,
+                     const FfmaGeneral gp) {
   constexpr int BM = T::BM, BN = T::BN, TY = T::TY, CG = T::CG;
+  constexpr int kStages = T::STAGES;
   // extents (elements) of C and of the partial tiles, for the checked build
   [[maybe_unused]] const size_t c_extent = stored_extent(p.M, p.N, GEN ? gp.ldc : p.N);
   [[maybe_unused]] const size_t work_extent =
@@ -226,18 +256,44 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
   extern __shared__ __align__(16) float smem_f[];
   __shared__ WorkItem pending[kMaxPending];   // split tiles this CTA must reduce
   __shared__ int pending_count;
-  float* const As = smem_f;                          // [stage][BM][kAPitch]
-  constexpr int kStages = T::STAGES;
-  float* const Bs = smem_f + kStages * T::A_STAGE;   // [stage][16][BN]
+  __shared__ __align__(8) uint64_t full_bar[kStages];   // TMA loads: stage filled
+  const uint32_t dyn0 = smem_addr(smem_f);
+  const uint32_t base = VEC ? (dyn0 + 1023u) & ~1023u : dyn0;
+  float* const As = smem_f + (base - dyn0) / 4;      // [stage][BM][16 or kAPitch]
+  constexpr int A_ST = VEC ? T::A_STAGE_TMA : T::A_STAGE;
+  float* const Bs = As + kStages * A_ST;             // [stage][B box][16][B_BOX]
   const uint32_t as_addr = smem_addr(As), bs_addr = smem_addr(Bs);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tx = (warp % T::WX) * T::LX + lane % T::LX;
   const int ty = (warp / T::WX) * (32 / T::LX) + lane / T::LX;
-  if (threadIdx.x == 0) pending_count = 0;
+  if (threadIdx.x == 0) {
+    pending_count = 0;
+    if (VEC) {
+      for (int st = 0; st < kStages; ++st) mbar_init(smem_addr(&full_bar[st]), 1);
+      fence_mbar_init();
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    }
+  }
+  __syncthreads();
+
+  // TMA loads: fills issued (thread 0) and stages consumed (every thread),
+  // counted over all work items, so stage = n % S and parity = (n / S) & 1
+  uint32_t fills = 0, uses = 0;
+  int dropped = -1;     // test hook: the stage that was never filled
+  bool ok = true;
+  const int sw = (ty >> 1) & 3;   // 64-byte swizzle phase of this thread's A rows
+  auto a_at_tma = [&](int i, int kg) { return (ty + TY * i) * kBK + ((kg ^ sw) << 2); };
+  auto a_at_copy = [&](int i, int kg) { return (ty + TY * i) * kAPitch + kg * 4; };
+  auto b_at_tma = [&](int k, int g) {
+    const int col = g * CG + tx * 4;
+    return (col / T::B_BOX) * (kBK * T::B_BOX) + k * T::B_BOX + col % T::B_BOX;
+  };
+  auto b_at_copy = [&](int k, int g) { return k * BN + g * CG + tx * 4; };
 
   WorkList list(p);
   WorkItem w;
-  while (list.next(p, w)) {
+  while (ok && list.next(p, w)) {
     const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
     const int m0 = c.tm * BM, n0 = c.tn * BN;
     const int nk = w.k1 - w.k0;
@@ -248,56 +304,71 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[i][q] = 0ull;
 
-    // prologue: the first kStages-1 tiles in flight (empty groups keep the count)
+    if constexpr (VEC) {
+      // one thread fills stage fills % S with K tile kt; the stage it
+      // overwrites was consumed at least one barrier ago
+      auto issue = [&](int kt) {
+        const uint32_t st = fills % kStages;
+        const uint32_t bar = smem_addr(&full_bar[st]);
+        if (p.drop_first_copy && blockIdx.x == 0 && fills == 0) {
+          dropped = 0;   // never armed: the waits on it run out
+        } else {
+          mbar_arrive_expect_tx(bar, T::STAGE_BYTES_TMA);
+          const uint32_t a_dst = as_addr + st * (T::A_STAGE_TMA * 4);
+          const uint32_t b_dst = bs_addr + st * (T::B_STAGE * 4);
 #pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-      if (s < nk)
-        load_stage<T, VEC, GEN>(p, gp, m0, n0, w.k0 + s, as_addr + s * T::A_STAGE * 4,
-                                bs_addr + s * T::B_STAGE * 4);
-      cp_async_commit();
-    }
-
-    for (int j = 0; j < nk; ++j) {
-      cp_async_wait<kStages - 2>();   // this thread's copies of tile j have landed
-      __syncthreads();                // everyone's have; stage (j-1) % S is free
-      const int nxt = j + kStages - 1;
-      if (nxt < nk) {
-        const int s = nxt % kStages;
-        load_stage<T, VEC, GEN>(p, gp, m0, n0, w.k0 + nxt, as_addr + s * T::A_STAGE * 4,
-                                bs_addr + s * T::B_STAGE * 4);
-      }
-      cp_async_commit();
-
-      const float* const as = As + (j % kStages) * T::A_STAGE;
-      const float* const bs = Bs + (j % kStages) * T::B_STAGE;
+          for (int h = 0; h < BM / T::A_BOX; ++h)
+            tma_load_2d(a_dst + h * (T::A_BOX * kBK * 4), &tmA, bar, kt * kBK, m0 + h * T::A_BOX);
 #pragma unroll
-      for (int kg = 0; kg < kBK / 4; ++kg) {
-        float4 a4[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          a4[i] = *reinterpret_cast<const float4*>(as + (ty + TY * i) * kAPitch + kg * 4);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint64_t b[8];
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const ulonglong2 v =
-                *reinterpret_cast<const ulonglong2*>(bs + (kg * 4 + kk) * BN + g * CG + tx * 4);
-            b[2 * g] = v.x;
-            b[2 * g + 1] = v.y;
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const float a = kk == 0 ? a4[i].x : kk == 1 ? a4[i].y : kk == 2 ? a4[i].z : a4[i].w;
-            const uint64_t aa = pair(a, a);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[i][q] = fma2(aa, b[q], acc[i][q]);
-          }
+          for (int h = 0; h < BN / T::B_BOX; ++h)
+            tma_load_2d(b_dst + h * (T::B_BOX * kBK * 4), &tmB, bar, n0 + h * T::B_BOX, kt * kBK);
         }
+        ++fills;
+      };
+      if (threadIdx.x == 0)
+        for (int st = 0; st < kStages - 1 && st < nk; ++st) issue(w.k0 + st);
+      for (int j = 0; j < nk; ++j) {
+        const uint32_t st = uses % kStages;
+        const bool got = mbar_wait(smem_addr(&full_bar[st]), (uses / kStages) & 1u, p.err,
+                                   kSiteTransformFull);
+        // every thread's copy of the verdict; also the barrier after which
+        // stage (j - 1) % S, read by the iteration before, may be refilled
+        if (!__syncthreads_and(got)) {
+          ok = false;
+          break;
+        }
+        if (threadIdx.x == 0 && j + kStages - 1 < nk) issue(w.k0 + j + kStages - 1);
+        stage_product<T>(As + st * T::A_STAGE_TMA, Bs + st * T::B_STAGE, a_at_tma, b_at_tma,
+                         acc);
+        ++uses;
       }
+      if (!ok) break;
+      __syncthreads();
+    } else {
+      // prologue: the first kStages-1 tiles in flight (empty groups keep the count)
+#pragma unroll
+      for (int st = 0; st < kStages - 1; ++st) {
+        if (st < nk)
+          load_stage<T, GEN>(p, gp, m0, n0, w.k0 + st, as_addr + st * T::A_STAGE * 4,
+                             bs_addr + st * T::B_STAGE * 4);
+        cp_async_commit();
+      }
+      for (int j = 0; j < nk; ++j) {
+        cp_async_wait<kStages - 2>();   // this thread's copies of tile j have landed
+        __syncthreads();                // everyone's have; stage (j-1) % S is free
+        const int nxt = j + kStages - 1;
+        if (nxt < nk) {
+          const int st = nxt % kStages;
+          load_stage<T, GEN>(p, gp, m0, n0, w.k0 + nxt, as_addr + st * T::A_STAGE * 4,
+                             bs_addr + st * T::B_STAGE * 4);
+        }
+        cp_async_commit();
+        stage_product<T>(As + (j % kStages) * T::A_STAGE, Bs + (j % kStages) * T::B_STAGE,
+                         a_at_copy, b_at_copy, acc);
+      }
+      cp_async_wait<0>();
+      __syncthreads();   // the next item's prologue overwrites stages still being read
     }
-    cp_async_wait<0>();
-    __syncthreads();   // the next item's prologue overwrites stages still being read
 
     if (w.nseg == 1) {
       // epilogue: rows ty + TY i, columns CG g + 4 tx .. +3
@@ -387,6 +458,18 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
     }
   }
 
+  if (!ok) {
+    // a wait ran out (reported in the error word): C of this call is left
+    // as it is; the loads still in flight land before the CTA's shared
+    // memory goes away
+    if (threadIdx.x == 0)
+      for (uint32_t f = uses; f < fills; ++f)
+        if (static_cast<int>(f) != dropped)
+          mbar_wait(smem_addr(&full_bar[f % kStages]), (f / kStages) & 1u, p.err, kSiteDrainTma);
+    __syncthreads();
+    if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
+    return;
+  }
   __syncthreads();
   const int npend = pending_count;
   if (npend > 0) {
@@ -422,11 +505,12 @@ int resident_ctas(int device) {
   int n = per_sm[d].load();
   if (n > 0) return n;
   auto kern = ffma_gemm_kernel<T, VEC, GEN>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM) !=
+  constexpr int smem = VEC ? T::SMEM_TMA : T::SMEM;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
           cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::THREADS, T::SMEM) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::THREADS, smem) != cudaSuccess ||
       n < 1) {
     (void)cudaGetLastError();
     return 0;
@@ -437,8 +521,10 @@ int resident_ctas(int device) {
 }
 
 template <class T, bool VEC, bool GEN>
-int launch_vec(const FfmaParams& p, const FfmaGeneral& gp, int grid, cudaStream_t stream) {
-  ffma_gemm_kernel<T, VEC, GEN><<<grid, T::THREADS, T::SMEM, stream>>>(p, gp);
+int launch_vec(const CUtensorMap& ma, const CUtensorMap& mb, const FfmaParams& p,
+               const FfmaGeneral& gp, int grid, cudaStream_t stream) {
+  ffma_gemm_kernel<T, VEC, GEN><<<grid, T::THREADS, VEC ? T::SMEM_TMA : T::SMEM, stream>>>(ma, mb, p,
+                                                                                          gp);
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;
 }
@@ -461,6 +547,7 @@ int launch_tile(GemmArgs& g, cudaStream_t stream, int* launches) {
   p.k_iters = (g.K + kBK - 1) / kBK;
   p.partials = nullptr;
   p.counters = nullptr;
+  p.drop_first_copy = (g.flags & GEMM_F32_FLAG_TEST_DROP_COPY) ? 1 : 0;
   p.err = g.err;
   FfmaGeneral gp;
   gp.lda = g.lda;
@@ -478,9 +565,16 @@ int launch_tile(GemmArgs& g, cudaStream_t stream, int* launches) {
   p.sk_ctas = 0;
   p.sk_work = 0;
   p.max_seg = 1;
-  // 16-byte copies: untransposed, strides a multiple of 4 floats, aligned
-  // bases, and K, N multiples of 4 (a chunk is wholly inside or outside)
-  const bool vec = tma_addressable(g) && g.K % 4 == 0 && g.N % 4 == 0;
+  // TMA loads: untransposed operands, row strides a multiple of 4 floats,
+  // 16-byte aligned bases (ragged edges read as zero); otherwise 4-byte copies
+  alignas(64) CUtensorMap ma, mb;
+  bool vec = tma_addressable(g) &&
+             tma_encode_2d(&ma, g.A, g.M, g.K, g.lda, kBK, T::A_BOX, CU_TENSOR_MAP_SWIZZLE_64B) &&
+             tma_encode_2d(&mb, g.B, g.K, g.N, g.ldb, T::B_BOX, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!vec) {
+    memset(&ma, 0, sizeof(ma));
+    memset(&mb, 0, sizeof(mb));
+  }
   const bool gen = !plain_form(g);
   const int per_sm = gen ? (vec ? resident_ctas<T, true, true>(g.device)
                                 : resident_ctas<T, false, true>(g.device))
@@ -505,11 +599,11 @@ int launch_tile(GemmArgs& g, cudaStream_t stream, int* launches) {
   }
   int rc;
   if (gen)
-    rc = vec ? launch_vec<T, true, true>(p, gp, grid, stream)
-             : launch_vec<T, false, true>(p, gp, grid, stream);
+    rc = vec ? launch_vec<T, true, true>(ma, mb, p, gp, grid, stream)
+             : launch_vec<T, false, true>(ma, mb, p, gp, grid, stream);
   else
-    rc = vec ? launch_vec<T, true, false>(p, gp, grid, stream)
-             : launch_vec<T, false, false>(p, gp, grid, stream);
+    rc = vec ? launch_vec<T, true, false>(ma, mb, p, gp, grid, stream)
+             : launch_vec<T, false, false>(ma, mb, p, gp, grid, stream);
   if (rc == GEMM_F32_OK) {
     *launches += 1;
     g.kernel = "ffma_gemm_kernel";

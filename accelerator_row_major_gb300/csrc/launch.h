@@ -2,6 +2,7 @@
 // kernel translation units.  Not installed; not part of the public ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -68,6 +69,12 @@ int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 int launch_tc_fixed_scratch(GemmArgs& g, int nprod, void* scratch, cudaStream_t stream,
                             int* launches);
 void* fixed_scratch_address();
+
+// 2-D fp32 tensor map of a row-major [rows x cols] matrix with row stride ld
+// (elements) and box [box_rows x box_cols]; out-of-bounds reads give zero.
+// False when the driver entry point or the encoding fails.
+bool tma_encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, int box_cols,
+                   int box_rows, CUtensorMapSwizzle swz);
 
 // CUDA-core FFMA path.
 int launch_ffma(GemmArgs& g, cudaStream_t stream, int* launches);

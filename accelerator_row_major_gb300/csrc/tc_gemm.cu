@@ -741,9 +741,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return g_encode;
 }
 
+}  // namespace
+
 // 2-D fp32 map of a row-major [rows x cols] matrix with row stride ld
-// (elements), box [box_rows x box_cols].
-bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, int box_cols,
+// (elements), box [box_rows x box_cols]; out-of-bounds boxes read as zero.
+bool tma_encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, int box_cols,
                int box_rows, CUtensorMapSwizzle swz) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encoder();
   if (!enc) return false;
@@ -755,6 +757,8 @@ bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, i
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+namespace {
 
 constexpr int kMaxDevices = 64;
 
@@ -1004,9 +1008,9 @@ int launch_tc_tn(GemmArgs& g, int nprod, int tn, const TailScratch& scratch, cud
   bool tma = tma_ok;
   alignas(64) CUtensorMap ma, mb;
   if (tma) {
-    tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, tm,
+    tma = tma_encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, tm,
                     bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, g.ldb, tn, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+          tma_encode_2d(&mb, g.B, g.K, g.N, g.ldb, tn, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!tma) {
     if (tn != kTN) return kRetryWide;

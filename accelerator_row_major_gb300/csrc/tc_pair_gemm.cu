@@ -738,31 +738,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool encode_2d(CUtensorMap* map, const float* ptr, int rows, int cols, int ld, int box_cols,
-               int box_rows, CUtensorMapSwizzle swz) {
-  std::call_once(g_encode_once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    else
-      (void)cudaGetLastError();
-  });
-  if (!g_encode) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 4u};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 constexpr int kMaxDevices = 64;
 
 template <int BK, int NPROD, int LOAD>
@@ -809,9 +784,9 @@ int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
   int bk = (nprod == 1 && tma) ? 32 : 16;
   alignas(64) CUtensorMap ma, mb;
   if (tma) {
-    tma = encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, kHalf,
+    tma = tma_encode_2d(&ma, g.A, g.M, g.K, g.lda, bk, kHalf,
                     bk == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B) &&
-          encode_2d(&mb, g.B, g.K, g.N, g.ldb, kHalf, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
+          tma_encode_2d(&mb, g.B, g.K, g.N, g.ldb, kHalf, bk, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!tma) {
     bk = 16;

@@ -101,14 +101,15 @@ enum gemm_f32_mode {
                                             two CTAs, one M = 256 MMA); the
                                             default for large M and N         */
 #define GEMM_F32_FLAG_SINGLE_CTA 0x800u  /* tensor modes: one CTA per tile    */
-#define GEMM_F32_FLAG_TEST_DROP_COPY 0x1000u /* testing only, tensor modes on
-                                            the TMA path: CTA 0 never issues
-                                            its first operand copy, so its
-                                            bounded waits run out (about 2 s)
-                                            and gemm_f32_status() returns
+#define GEMM_F32_FLAG_TEST_DROP_COPY 0x1000u /* testing only, on the TMA
+                                            path of every mode: CTA 0 never
+                                            issues its first operand copy, so
+                                            its bounded waits run out (about
+                                            2 s) and gemm_f32_status() returns
                                             GEMM_F32_ETIMEOUT.  C is undefined
-                                            after such a call.  Ignored by the
-                                            FFMA mode, which has no waits.    */
+                                            after such a call.  Ignored where
+                                            operands are copied per thread
+                                            (no waits there).                 */
 
 /* Small products: without flags, a product of at most 2^23 multiply-adds
  * with K <= 256 runs in every mode on a CUDA-core kernel (fp32 fused

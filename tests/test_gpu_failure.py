@@ -16,7 +16,7 @@ from tests._gpu import TOL, assert_close, lib, oracle_full, run_abi
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mode,extra", [("tc3x", 0), ("tc1x", 0), ("tc3x", 0x400)])
+@pytest.mark.parametrize("mode,extra", [("tc3x", 0), ("tc1x", 0), ("tc3x", 0x400), ("ffma", 0)])
 def test_lost_copy_reports_timeout_and_context_survives(mode, extra):
     import torch
 
@@ -42,23 +42,24 @@ def test_lost_copy_reports_timeout_and_context_survives(mode, extra):
     assert_close(C2, Co, absAB, TOL[mode], "after timeout/%s" % mode)
 
 
-def test_ffma_ignores_the_test_flag():
+def test_per_thread_copies_ignore_the_test_flag():
+    # an odd K keeps FFMA on its per-thread copies, which have no waits
     g = lib()
-    A, B = workloads.make_inputs(200, 64, 136, "uniform", 9)
+    A, B = workloads.make_inputs(200, 63, 136, "uniform", 9)
     Co, absAB = oracle_full(A, B)
     C, _ = run_abi(A, B, "ffma", g.FLAG_TEST_DROP_COPY)
     assert_close(C, Co, absAB, TOL["ffma"], "ffma with test flag")
 
 
-@pytest.mark.parametrize("mode,flags", [("tc3x", 0), ("tc3x", 0x800), ("tc1x", 0)])
+@pytest.mark.parametrize("mode,flags", [("tc3x", 0), ("tc3x", 0x800), ("tc1x", 0), ("ffma", 0)])
 def test_split_tail_after_a_timeout_needs_no_status_call(mode, flags):
     """A split-tail call whose bounded waits run out leaves some tile
     counters of its workspace half counted (CTA 0 never publishes its
     partials).  The next split-tail call on the same stream, made without
     gemm_f32_status() in between, must still pick the right CTA to sum each
     tile: its whole C is compared with the oracle.  3000 x 4096 x 2000
-    splits its last wave along K on the CTA-pair kernel (default) and on the
-    single-CTA kernel (0x800)."""
+    splits its last wave along K on the CTA-pair kernel (default), on the
+    single-CTA kernel (0x800) and on the FFMA kernel's TMA path."""
     import torch
 
     g = lib()
