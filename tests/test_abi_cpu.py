@@ -42,6 +42,20 @@ def test_library_exports_every_declared_symbol(g):
 def test_version(g):
     assert g.gemm_f32_version().startswith("gemm_f32 ")
     assert "sm_103a" in g.gemm_f32_version()
+    assert not g.gemm_f32_version().endswith("bounds-checked")   # the default build
+
+
+def test_unit_rates_rejects_a_null_record(g):
+    from accelerator_row_major_gb300 import _binding
+    assert _binding.lib().gemm_f32_unit_rates(None) == g.GEMM_F32_EINVAL
+
+
+def test_tile224_flag_is_known_and_exclusive(g):
+    # 224-row tiles are a tile-height flag like the others: accepted alone
+    # (the call then stops at the device check), refused with another height
+    args = (FAKE_A, FAKE_B, FAKE_C, 4, 4, 4)
+    assert g.gemm_f32_ex(*args, mode=0, flags=0x80) != g.GEMM_F32_EINVAL
+    assert g.gemm_f32_ex(*args, mode=0, flags=0x80 | 0x40) == g.GEMM_F32_EINVAL
 
 
 FAKE_A, FAKE_B, FAKE_C = 0x100000, 0x200000, 0x300000

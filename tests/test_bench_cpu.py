@@ -100,3 +100,56 @@ def test_oracle_table_rows(capsys, monkeypatch):
         assert r["seconds"] > 0 and r["tflops"] > 0 and r["timing"] == "measured"
         assert (r["M"], r["K"], r["N"]) == (100, 37, 70)
         assert r["host_cores"] == cores >= 1 and r["cpu_model"] == model
+
+
+RATES = {"tf32_flop_per_clk_sm": 4000.0, "tf32_pair_flop_per_clk_sm": 4096.0,
+         "ffma_flop_per_clk_sm": 250.0, "sm_mhz": 1500.0, "num_sms": 100}
+PEAKS = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+
+
+def test_roofline_takes_the_probed_rate_times_the_sampled_clock():
+    clocks = {"sm_mhz": 2000.0, "window": "timed steps"}
+    flop, nbytes = 2 * 8192 ** 3, 4 * 3 * 8192 ** 2
+    pair = bench.roofline("tc_pair_kernel", "tc3x", flop, nbytes, 1e-3, RATES, clocks, PEAKS, "measured")
+    assert pair["bound"] == "tensor"
+    assert abs(pair["peak"] - 4096.0 * 100 * 2000e6 / 1e12) < 1e-9          # pair rate x SMs x clock
+    assert abs(pair["achieved"] - 3 * flop / 1e-3 / 1e12) < 1e-6            # three products per FLOP
+    assert abs(pair["frac"] - pair["achieved"] / pair["peak"]) < 1e-12
+    assert abs(pair["secondary"]["peak"] - 2000.0 * 1.1 / 2.25) < 1e-9
+    single = bench.roofline("tc_gemm_kernel", "tc1x", flop, nbytes, 1e-3, RATES, clocks, PEAKS, "measured")
+    assert abs(single["peak"] - 4000.0 * 100 * 2000e6 / 1e12) < 1e-9       # single-SM rate
+    assert abs(single["achieved"] - flop / 1e-3 / 1e12) < 1e-6               # one product
+    ffma = bench.roofline("ffma_gemm_kernel", "ffma", flop, nbytes, 1e-3, RATES, clocks, PEAKS, "measured")
+    assert ffma["bound"] == "alu" and abs(ffma["peak"] - 250.0 * 100 * 2000e6 / 1e12) < 1e-9
+    # no clock samples: the clock the probe saw
+    noclk = bench.roofline("ffma_gemm_kernel", "ffma", flop, nbytes, 1e-3, RATES, None, PEAKS, "measured")
+    assert abs(noclk["peak"] - 250.0 * 100 * 1500e6 / 1e12) < 1e-9
+
+
+def test_roofline_of_a_skinny_shape_is_memory_bound():
+    M, K, N = 65536, 1024, 64
+    flop, nbytes = 2 * M * N * K, 4 * (M * K + K * N + M * N)
+    r = bench.roofline("tc_gemm_kernel", "tc3x", flop, nbytes, 60e-6, RATES,
+                       {"sm_mhz": 2000.0, "window": "timed steps"}, PEAKS, "measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6000.0
+    assert abs(r["achieved"] - nbytes / 60e-6 / 1e9) < 1e-6
+
+
+def _smi_line(t, mhz, cap="Not Active"):
+    import datetime
+    stamp = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return "%s, 0, %d, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, %s" % (stamp, mhz, cap)
+
+
+def test_clock_summary_takes_the_timed_window():
+    s = bench.ClockSampler(0, enabled=False)
+    t0 = 1_800_000_000.0
+    s.lines = [_smi_line(t0 + 0.02 * i, 2070 if i < 10 else 1700, "Active" if i >= 12 else "Not Active")
+               for i in range(20)]
+    inside = s.summary(t0 + 0.2, t0 + 0.4)             # samples 10 .. 20
+    assert inside["window"] == "timed steps" and inside["sm_mhz"] == 1700
+    assert inside["reasons"] == ["sw_power_cap"] and inside["samples"] >= 3
+    short = s.summary(t0 + 0.05, t0 + 0.07)             # fewer than 3 samples inside
+    assert short["window"].startswith("warm-up and timed steps")
+    assert short["sm_mhz"] == 2070 and short["samples"] == 4
+    assert bench.ClockSampler(0, enabled=False).summary() is None
