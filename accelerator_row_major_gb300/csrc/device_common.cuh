@@ -378,6 +378,25 @@ __device__ __forceinline__ void reduce_partials_general(const float* parts, int 
   }
 }
 
+// ---------------------------------------------------------------- dependent launches
+// Programmatic dependent launch: a kernel launched after one of these on the
+// same stream (with the programmatic-serialization launch attribute) may
+// start its CTAs as this one's CTAs finish.  Each kernel calls
+// grid_launch_dependents() once its own set-up is done, and
+// grid_dependency_wait() before its first global memory access: that wait
+// returns once every earlier kernel of the stream has completed and its
+// memory operations are visible, so a kernel may read what the previous one
+// wrote (C becoming the next A, the split tail's counters).  Only set-up that
+// touches nothing global (barriers, tensor memory, descriptor prefetch) runs
+// before it.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- shared memory
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

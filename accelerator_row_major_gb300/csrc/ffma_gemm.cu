@@ -276,6 +276,8 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
     }
   }
   __syncthreads();
+  grid_launch_dependents();
+  grid_dependency_wait();   // global memory from here on
 
   // TMA loads: fills issued (thread 0) and stages consumed (every thread),
   // counted over all work items, so stage = n % S and parity = (n / S) & 1
@@ -523,9 +525,11 @@ int resident_ctas(int device) {
 template <class T, bool VEC, bool GEN>
 int launch_vec(const CUtensorMap& ma, const CUtensorMap& mb, const FfmaParams& p,
                const FfmaGeneral& gp, int grid, cudaStream_t stream) {
-  ffma_gemm_kernel<T, VEC, GEN><<<grid, T::THREADS, VEC ? T::SMEM_TMA : T::SMEM, stream>>>(ma, mb, p,
-                                                                                          gp);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  if (launch_dependent(ffma_gemm_kernel<T, VEC, GEN>, dim3(grid), dim3(T::THREADS),
+                       VEC ? T::SMEM_TMA : T::SMEM, stream, ma, mb, p, gp) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
   return GEMM_F32_OK;
 }
 

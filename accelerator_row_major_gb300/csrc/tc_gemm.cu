@@ -297,6 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(base_ptr + (tmem_slot - base));
+  grid_launch_dependents();
+  grid_dependency_wait();   // global memory from here on
 
   WorkItem w;
   if (warp == 0) {
@@ -777,8 +779,11 @@ int launch_one(const GemmArgs& g, const TcParams& p, const TcGeneral& gp, const 
     }
     configured.fetch_or(bit);
   }
-  kern<<<grid, kThreads, Cfg::SMEM, stream>>>(ma, mb, p, gp);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  if (launch_dependent(kern, dim3(grid), dim3(kThreads), Cfg::SMEM, stream, ma, mb, p, gp) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
   return GEMM_F32_OK;
 }
 
