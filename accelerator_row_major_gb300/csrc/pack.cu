@@ -46,6 +46,8 @@ __device__ __forceinline__ size_t dst_extent(const RowCopy& m) {
 }
 
 __global__ void pack_rows_kernel(RowCopy x, RowCopy y, unsigned* err) {
+  grid_launch_dependents();   // the product after this copy may start its set-up
+  grid_dependency_wait();
   const long long nx = static_cast<long long>(x.rows) * x.cols;
   const long long total = nx + static_cast<long long>(y.rows) * y.cols;
   for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
@@ -69,8 +71,12 @@ int launch_rows(const RowCopy& x, const RowCopy& y, int num_sms, unsigned* err,
   const long long total = static_cast<long long>(x.rows) * x.cols + static_cast<long long>(y.rows) * y.cols;
   const long long want = (total + 255) / 256;
   const int grid = static_cast<int>(want < 8LL * num_sms ? want : 8LL * num_sms);
-  pack_rows_kernel<<<grid, 256, 0, stream>>>(x, y, err);
-  return cudaGetLastError() == cudaSuccess ? GEMM_F32_OK : GEMM_F32_ELAUNCH;
+  if (launch_dependent(pack_rows_kernel, dim3(grid), dim3(256), 0, stream, x, y, err) !=
+      cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
+  return GEMM_F32_OK;
 }
 
 RowCopy row_copy(const float* src, int rows, int cols, int ld_src, float* dst, int ld_dst) {
@@ -89,6 +95,8 @@ __global__ void pack_transpose_kernel(const float* __restrict__ src, int rows, i
                                       long long ld_src, float* __restrict__ dst, long long ld_dst,
                                       unsigned* err) {
   __shared__ float tile[kTile][kTile + 1];
+  grid_launch_dependents();
+  grid_dependency_wait();
   const int r0 = blockIdx.y * kTile, c0 = blockIdx.x * kTile;
   // read src rows c0.. (dst columns), lanes along src columns (dst rows)
   for (int y = threadIdx.y; y < kTile; y += blockDim.y) {
@@ -120,8 +128,12 @@ int pack_operand(const float* src, int rows, int cols, int ld_src, bool transpos
     const long long gy = (rows + kTile - 1) / kTile;
     if (gy > 65535) return GEMM_F32_EINVAL;
     const dim3 grid((cols + kTile - 1) / kTile, static_cast<unsigned>(gy));
-    pack_transpose_kernel<<<grid, dim3(kTile, 8), 0, stream>>>(src, rows, cols, ld_src, dst, ld_dst,
-                                                              err);
+    if (launch_dependent(pack_transpose_kernel, grid, dim3(kTile, 8), 0, stream, src, rows, cols,
+                         static_cast<long long>(ld_src), dst, static_cast<long long>(ld_dst),
+                         err) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return GEMM_F32_ELAUNCH;
+    }
   }
   if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
   return GEMM_F32_OK;

@@ -33,6 +33,8 @@ __global__ void __launch_bounds__(kT * kT) small_gemm_kernel(const float* __rest
                                                              int K, unsigned* err) {
   __shared__ float as[kT][kT];
   __shared__ float bs[kT][kT];
+  grid_launch_dependents();
+  grid_dependency_wait();   // global memory from here on
   const int tx = threadIdx.x, ty = threadIdx.y;
   const int i = blockIdx.y * kT + ty;
   const int j = blockIdx.x * kT + tx;
@@ -68,8 +70,11 @@ bool small_suits(const GemmArgs& g) {
 int launch_small(GemmArgs& g, cudaStream_t stream, int* launches) {
   *launches = 0;
   const dim3 grid((g.N + kT - 1) / kT, (g.M + kT - 1) / kT);
-  small_gemm_kernel<<<grid, dim3(kT, kT), 0, stream>>>(g.A, g.B, g.C, g.M, g.N, g.K, g.err);
-  if (cudaGetLastError() != cudaSuccess) return GEMM_F32_ELAUNCH;
+  if (launch_dependent(small_gemm_kernel, grid, dim3(kT, kT), 0, stream, g.A, g.B, g.C, g.M, g.N,
+                       g.K, g.err) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
   *launches = 1;
   g.kernel = "small_gemm_kernel";
   return GEMM_F32_OK;
