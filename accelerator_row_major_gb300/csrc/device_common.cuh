@@ -84,7 +84,10 @@ struct TileCoord {
   int tm, tn;
 };
 
-__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n, int group) {
+// With `snake`, odd groups run their columns right to left, so that the
+// last tiles of one group and the first of the next share B column panels.
+__device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n, int group,
+                                                bool snake = false) {
   const int per_group = group * tiles_n;
   const int g = t / per_group;
   const int first_m = g * group;
@@ -93,6 +96,7 @@ __device__ __forceinline__ TileCoord tile_coord(int t, int tiles_m, int tiles_n,
   TileCoord c;
   c.tm = first_m + r % rows_here;
   c.tn = r / rows_here;
+  if (snake && (g & 1)) c.tn = tiles_n - 1 - c.tn;
   return c;
 }
 
@@ -171,7 +175,14 @@ struct WorkItem {
   int tile, k0, k1;
   int tail;        // index among the split tiles, or -1 for a whole tile
   int seg, nseg;   // this CTA's position among the CTAs sharing the tile
+  bool rev;        // K iterations visited from k1 - 1 down to k0
 };
+
+// K iteration (tile column of A, tile row of B) that the n-th step of a work
+// item loads, n = kt - k0 counted from the item's first step.
+__device__ __forceinline__ int k_tile_at(const WorkItem& w, int kt) {
+  return w.rev ? w.k0 + w.k1 - 1 - kt : kt;
+}
 
 __host__ __device__ __forceinline__ long long sk_start(long long c, long long ctas, long long work) {
   return c * work / ctas;
@@ -206,6 +217,7 @@ struct WorkList {
       w.tail = -1;
       w.seg = 0;
       w.nseg = 1;
+      w.rev = false;
       next_dp += gridDim.x;
       return true;
     }
@@ -220,6 +232,7 @@ struct WorkList {
       const int last = sk_owner((i + 1) * ki - 1, p.sk_ctas, p.sk_work);
       w.seg = static_cast<int>(blockIdx.x) - first;
       w.nseg = last - first + 1;
+      w.rev = false;
       x += w.k1 - w.k0;
       return true;
     }

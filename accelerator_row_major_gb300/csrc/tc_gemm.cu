@@ -265,6 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // split tiles this CTA published last, reduced after the work list
   volatile int* const pending_count = reinterpret_cast<volatile int*>(base_ptr + (tmem_slot + 8u - base));
   WorkItem* const pending = reinterpret_cast<WorkItem*>(base_ptr + (tmem_slot + 16u - base));
+  static_assert(8 * (3 * S + 2 * NACC + 2) + 16 + kMaxPending * sizeof(WorkItem) <= 1024,
+                "barriers and pending work fit the 1024 bytes after the stages");
   // LSTACK: the epilogue's exchange of B-lo sums, [64 columns][33] floats
   float* const xchg = reinterpret_cast<float*>(base_ptr + S * Cfg::STAGE_BYTES + 1024);
 

@@ -277,6 +277,10 @@ struct PairWorkList {
       w.tail = -1;
       w.seg = 0;
       w.nseg = 1;
+      // Odd waves walk K backwards: they start on the K slices the previous
+      // wave read last, which are still in L2, and the A row panels a wave
+      // shares with the one before it are then read mostly from L2.
+      w.rev = ((next_dp / units) & 1) != 0;
       next_dp += units;
       return true;
     }
@@ -291,6 +295,7 @@ struct PairWorkList {
       const int last = sk_owner((i + 1) * ki - 1, p.sk_ctas, p.sk_work);
       w.seg = unit - first;
       w.nseg = last - first + 1;
+      w.rev = false;
       x += w.k1 - w.k0;
       return true;
     }
@@ -335,6 +340,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* const pending_count =
       reinterpret_cast<volatile int*>(base_ptr + (tmem_slot + 8u - base));
   WorkItem* const pending = reinterpret_cast<WorkItem*>(base_ptr + (tmem_slot + 16u - base));
+  static_assert(8 * (4 * S + 3) + 16 + kMaxPending * sizeof(WorkItem) <= 1024,
+                "barriers and pending work fit the 1024 bytes after the stages");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -379,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true, first = true;
       PairWorkList list(p);
       while (ok && list.next(p, w)) {
-        const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+        const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup, true);
         for (int kt = w.k0; kt < w.k1; ++kt) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteProducerEmpty)) {
             ok = false;
@@ -398,9 +405,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(full_bar(s), Cfg::A_BYTES + Cfg::B_RAW_BYTES);
           armed |= 1u << s;
           last_ph = (last_ph & ~(1u << s)) | (ph << s);
-          tma_load_2d(st, &tmA, full_bar(s), kt * BK, c.tm * kPairTile + static_cast<int>(rank) * kHalf);
+          const int kc = k_tile_at(w, kt) * BK;
+          tma_load_2d(st, &tmA, full_bar(s), kc, c.tm * kPairTile + static_cast<int>(rank) * kHalf);
           tma_load_2d(st + Cfg::A_BYTES + Cfg::A_LO_BYTES, &tmB, full_bar(s),
-                      c.tn * kPairTile + static_cast<int>(rank) * kHalf, kt * BK);
+                      c.tn * kPairTile + static_cast<int>(rank) * kHalf, kc);
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -492,7 +500,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t acc_ph = 0;
     PairWorkList list(p);
     while (list.next(p, w)) {
-      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup, true);
       if (!epilogue_all(mbar_wait(accf_bar, acc_ph, p.err, kSiteEpilogueFull))) break;
       tc_fence_after_sync();
       const uint32_t t_acc = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
@@ -570,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     PairWorkList list(p);
     while (ok && list.next(p, w)) {
-      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      const TileCoord c = tile_coord(w.tile, p.tiles_m, p.tiles_n, kRasterGroup, true);
       for (int kt = w.k0; kt < w.k1; ++kt) {
         uint8_t* const st = base_ptr + s * Cfg::STAGE_BYTES;
         if (!mbar_wait(empty_bar(s), ph ^ 1u, p.err, kSiteTransformEmpty)) {
@@ -605,7 +613,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         } else {
           const int m0 = c.tm * kPairTile + static_cast<int>(rank) * kHalf;
           const int n0 = c.tn * kPairTile + static_cast<int>(rank) * kHalf;
-          const int k0 = kt * BK;
+          const int k0 = k_tile_at(w, kt) * BK;
           // This thread's loads for the stage are all issued before any of
           // them is used, so one latency covers the stage.
           constexpr int AV = kHalf * BK / (kTransformWarps * 32);   // 8
@@ -686,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __threadfence();
     for (int e = 0; e < npend; ++e) {
       const WorkItem pw = pending[e];
-      const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup);
+      const TileCoord c = tile_coord(pw.tile, p.tiles_m, p.tiles_n, kRasterGroup, true);
       const float4* const parts = reinterpret_cast<const float4*>(p.partials) +
                                   static_cast<size_t>(pw.tail) * p.max_seg * 2 * (kPairTile * kHalf / 4);
       constexpr int kVec = kPairTile * kHalf / 4;   // float4s of one half partial
