@@ -129,7 +129,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 20 ms while active,
+    """nvidia-smi clocks and throttle reasons sampled every 10 ms while active,
     each sample with its timestamp, so that the samples of a window (the
     timed steps) can be told from the rest (warm-up)."""
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -137,7 +137,7 @@ class ClockSampler:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, index: int, enabled: bool = True, period_ms: int = 20):
+    def __init__(self, index: int, enabled: bool = True, period_ms: int = 10):
         self.index = index
         self.proc = None
         self.enabled = enabled
@@ -200,9 +200,16 @@ class ClockSampler:
             rows = inside or rows
         reasons = sorted({self.REASONS[i] for _, _, _, flags in rows for i, v in enumerate(flags)
                           if v == "Active"})
-        return {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
-                "reasons": reasons, "samples": len(rows), "window": window,
-                "period_ms": self.period_ms}
+        out = {"sm_mhz": statistics.median(r[1] for r in rows), "sm_max_mhz": max(r[2] for r in rows),
+               "reasons": reasons, "samples": len(rows), "window": window,
+               "period_ms": self.period_ms}
+        if t1 is not None:
+            # the wider record: warm-up and timed steps together
+            wide = [r for r in self.samples() if r[0] <= t1]
+            if wide:
+                out["with_warmup"] = {"sm_mhz": statistics.median(r[1] for r in wide),
+                                      "min_sm_mhz": min(r[1] for r in wide), "samples": len(wide)}
+        return out
 
 
 # the sources each kernel's device code comes from: its own file and the

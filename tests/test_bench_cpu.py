@@ -152,4 +152,6 @@ def test_clock_summary_takes_the_timed_window():
     short = s.summary(t0 + 0.05, t0 + 0.07)             # fewer than 3 samples inside
     assert short["window"].startswith("warm-up and timed steps")
     assert short["sm_mhz"] == 2070 and short["samples"] == 4
+    # the wider record covers every sample up to the end of the timed steps
+    assert inside["with_warmup"]["samples"] == 20 and inside["with_warmup"]["min_sm_mhz"] == 1700
     assert bench.ClockSampler(0, enabled=False).summary() is None
