@@ -283,6 +283,49 @@ struct BoundsRef {
   size_t c_extent;
 };
 
+// sum[i] += chunk `base` + i of each of the nseg partial tiles at p4, in
+// segment order.  The loads of two segments are issued together, so that a
+// chunk of the usual two-segment tile costs one round trip to L2, not two.
+template <int kChunk, int kVec, int NTHREADS>
+__device__ __forceinline__ void add_segments(const float4* p4, int nseg, int base,
+                                             float4 (&sum)[kChunk],
+                                             [[maybe_unused]] const BoundsRef& br) {
+  auto load = [&](int sg, int i) {
+    const size_t f4 = static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS;
+    return GEMM_IN_EXTENT(4 * f4 + 3, br.parts_extent, br.err, kSiteBoundsWork)
+               ? __ldcg(p4 + f4)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  auto add = [&](float4& a, const float4& x) {
+    a.x += x.x;
+    a.y += x.y;
+    a.z += x.z;
+    a.w += x.w;
+  };
+  int sg = 0;
+#pragma unroll 1
+  for (; sg + 1 < nseg; sg += 2) {
+    float4 x0[kChunk], x1[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      x0[i] = load(sg, i);
+      x1[i] = load(sg + 1, i);
+    }
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) {
+      add(sum[i], x0[i]);
+      add(sum[i], x1[i]);
+    }
+  }
+  if (sg < nseg) {
+    float4 x0[kChunk];
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) x0[i] = load(sg, i);
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i) add(sum[i], x0[i]);
+  }
+}
+
 template <int ROWS, int COLS, int NTHREADS, int CHUNK>
 __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, int m0, int n0,
                                                 int M, int N, float* C,
@@ -297,24 +340,7 @@ __device__ __forceinline__ void reduce_partials(const float* parts, int nseg, in
     float4 sum[kChunk];
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int sg = 0; sg < nseg; ++sg) {
-      float4 x[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const size_t f4 = static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS;
-        x[i] = GEMM_IN_EXTENT(4 * f4 + 3, br.parts_extent, br.err, kSiteBoundsWork)
-                   ? __ldcg(p4 + f4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        sum[i].x += x[i].x;
-        sum[i].y += x[i].y;
-        sum[i].z += x[i].z;
-        sum[i].w += x[i].w;
-      }
-    }
+    add_segments<kChunk, kVec, NTHREADS>(p4, nseg, base, sum, br);
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const int f = threadIdx.x + (base + i) * NTHREADS;   // float4 index in the tile
@@ -349,24 +375,7 @@ __device__ __forceinline__ void reduce_partials_general(const float* parts, int 
     float4 sum[kChunk];
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) sum[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-    for (int sg = 0; sg < nseg; ++sg) {
-      float4 x[kChunk];
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        const size_t f4 = static_cast<size_t>(sg) * kVec + threadIdx.x + (base + i) * NTHREADS;
-        x[i] = GEMM_IN_EXTENT(4 * f4 + 3, br.parts_extent, br.err, kSiteBoundsWork)
-                   ? __ldcg(p4 + f4)
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int i = 0; i < kChunk; ++i) {
-        sum[i].x += x[i].x;
-        sum[i].y += x[i].y;
-        sum[i].z += x[i].z;
-        sum[i].w += x[i].w;
-      }
-    }
+    add_segments<kChunk, kVec, NTHREADS>(p4, nseg, base, sum, br);
 #pragma unroll
     for (int i = 0; i < kChunk; ++i) {
       const int f = threadIdx.x + (base + i) * NTHREADS;   // float4 index in the tile

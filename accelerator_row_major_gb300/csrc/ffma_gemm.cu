@@ -483,12 +483,12 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
       const float* parts = p.partials + at;
       const BoundsRef br{p.err, work_extent - at, c_extent};
       if constexpr (!GEN)
-        reduce_partials<BM, BN, T::THREADS, 8>(parts, pw.nseg, c.tm * BM, c.tn * BN, p.M, p.N,
-                                               p.C, br);
+        reduce_partials<BM, BN, T::THREADS, 16>(parts, pw.nseg, c.tm * BM, c.tn * BN, p.M, p.N,
+                                                p.C, br);
       else
-        reduce_partials_general<BM, BN, T::THREADS, 8>(parts, pw.nseg, c.tm * BM, c.tn * BN,
-                                                       p.M, p.N, p.C, gp.ldc, gp.scale, gp.alpha,
-                                                       gp.beta, br);
+        reduce_partials_general<BM, BN, T::THREADS, 16>(parts, pw.nseg, c.tm * BM, c.tn * BN,
+                                                        p.M, p.N, p.C, gp.ldc, gp.scale, gp.alpha,
+                                                        gp.beta, br);
     }
   }
   if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
