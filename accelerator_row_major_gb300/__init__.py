@@ -16,7 +16,7 @@ from ._binding import (FLAG_CTA_PAIR, FLAG_FORCE_STAGED, FLAG_SINGLE_CTA, FLAG_T
                        gemm_f32, gemm_f32_ex, gemm_f32_general, gemm_f32_host, gemm_f32_ladder, gemm_f32_last_kernel, gemm_f32_last_launches,
                        gemm_f32_noalloc, LADDER_STEPS,
                        gemm_f32_release, NOALLOC_SCRATCH_BYTES,
-                       gemm_f32_status, gemm_f32_unit_rates,
+                       gemm_f32_clock_record, gemm_f32_status, gemm_f32_unit_rates,
                        gemm_f32_version)
 
 

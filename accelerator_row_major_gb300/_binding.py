@@ -94,6 +94,9 @@ def _load() -> ctypes.CDLL:
     lib.gemm_f32_version.restype = ctypes.c_char_p
     lib.gemm_f32_unit_rates.argtypes = [ctypes.POINTER(UnitRates)]
     lib.gemm_f32_unit_rates.restype = ci
+    u64p = ctypes.POINTER(ctypes.c_ulonglong)
+    lib.gemm_f32_clock_record.argtypes = [vp, u64p, u64p]
+    lib.gemm_f32_clock_record.restype = ci
     return lib
 
 
@@ -188,6 +191,17 @@ def gemm_f32_status(stream=None):
     site = ctypes.c_uint(0)
     rc = lib().gemm_f32_status(_stream(stream), ctypes.byref(site))
     return rc, site.value
+
+
+def gemm_f32_clock_record(stream=None):
+    """(sm_cycles, ns): the device's running sums of CTA 0's lifetime over the
+    persistent kernels' launches (synchronises the stream); the difference of
+    two readings gives the SM clock in between, cycles / ns GHz.  Raises
+    GemmError on failure."""
+    cycles, ns = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    check(lib().gemm_f32_clock_record(_stream(stream), ctypes.byref(cycles), ctypes.byref(ns)),
+          "gemm_f32_clock_record")
+    return cycles.value, ns.value
 
 
 def gemm_f32_last_launches() -> int:

@@ -37,6 +37,40 @@ __device__ __forceinline__ void record_error(unsigned* err, unsigned site) {
   atomicCAS(err, 0u, site);
 }
 
+// ---------------------------------------------------------------- clock record
+// The error word is the first of a 32-byte block of device words; bytes
+// 16..31 hold two 64-bit sums, the clock record.  The first thread of CTA 0
+// of the pair and FFMA kernels adds its CTA's lifetime to them, in SM clocks
+// (clock64) and in nanoseconds (%globaltimer).  CTA 0 of a persistent grid
+// lives through the whole launch, so cycles / ns over a run of launches is
+// the SM clock they ran at, whatever the driver's sampled clock says.  The
+// start mark is kept in shared memory, so the record holds no register
+// through the kernel.
+struct ClockRecord {
+  unsigned long long cycles, ns;
+};
+
+__device__ __forceinline__ ClockRecord* clock_record(unsigned* err) {
+  return reinterpret_cast<ClockRecord*>(err + 4);
+}
+
+__device__ __forceinline__ void clock_start(unsigned long long (&mark)[2]) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    mark[0] = clock64();
+    mark[1] = globaltimer_ns();
+  }
+}
+
+__device__ __forceinline__ void clock_stop(unsigned* err, const unsigned long long (&mark)[2]) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const unsigned long long c = clock64() - mark[0];
+    const unsigned long long t = globaltimer_ns() - mark[1];
+    ClockRecord* const r = clock_record(err);
+    atomicAdd(&r->cycles, c);
+    atomicAdd(&r->ns, t);
+  }
+}
+
 // ---------------------------------------------------------------- bounds checks
 // The debug build (-DGEMM_BOUNDS_CHECK, libgemm_f32_checked.so) checks every
 // global load and store that a kernel indexes by hand -- the per-thread

@@ -257,6 +257,8 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
   __shared__ WorkItem pending[kMaxPending];   // split tiles this CTA must reduce
   __shared__ int pending_count;
   __shared__ __align__(8) uint64_t full_bar[kStages];   // TMA loads: stage filled
+  __shared__ unsigned long long clk_mark[2];            // the clock record's start
+  clock_start(clk_mark);
   const uint32_t dyn0 = smem_addr(smem_f);
   const uint32_t base = VEC ? (dyn0 + 1023u) & ~1023u : dyn0;
   float* const As = smem_f + (base - dyn0) / 4;      // [stage][BM][16 or kAPitch]
@@ -469,6 +471,7 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
         if (static_cast<int>(f) != dropped)
           mbar_wait(smem_addr(&full_bar[f % kStages]), (f / kStages) & 1u, p.err, kSiteDrainTma);
     __syncthreads();
+    clock_stop(p.err, clk_mark);
     if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
     return;
   }
@@ -491,6 +494,7 @@ __global__ void __launch_bounds__(T::THREADS, T::CTAS_PER_SM)
                                                         gp.beta, br);
     }
   }
+  clock_stop(p.err, clk_mark);
   if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
 }
 

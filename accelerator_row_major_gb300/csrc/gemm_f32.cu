@@ -18,9 +18,13 @@
 
 namespace {
 
-// One error word per device: 0, or the site code of the first bounded wait
-// that ran out since the last gemm_f32_status() on that device.
-__device__ unsigned g_error_word;
+// One block of device words per device.  Word 0 is the error word: 0, or
+// the site code of the first bounded wait (or, in the checked build, the
+// first out-of-range index) since the last gemm_f32_status() on that device.
+// Words 4..7 are the clock record (two 64-bit sums, SM clocks and
+// nanoseconds of CTA 0 of each pair and FFMA launch), read by
+// gemm_f32_clock_record().
+__device__ __align__(16) unsigned g_device_words[8];
 
 constexpr int kMaxDevices = 64;
 
@@ -35,7 +39,7 @@ struct DeviceState {
   std::once_flag once;
   int status = GEMM_F32_EDEVICE;  // GEMM_F32_OK once set up
   int num_sms = 0;
-  unsigned* err = nullptr;        // device address of g_error_word
+  unsigned* err = nullptr;        // device address of g_device_words
   std::mutex fixed_mu;
   void* fixed_scratch = nullptr;  // device address of gemm_f32_noalloc's array
   std::mutex ws_mu;
@@ -70,12 +74,12 @@ DeviceState* device_state(int* device_out) {
     }
     if (major != 10 || minor != 3) return;  // the kernels are built for sm_103a only
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) {
+    if (cudaGetSymbolAddress(&p, g_device_words) != cudaSuccess) {
       (void)cudaGetLastError();
       return;
     }
-    const unsigned zero = 0;
-    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
+    const unsigned zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (cudaMemcpy(p, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) {
       (void)cudaGetLastError();
       return;
     }
@@ -589,6 +593,28 @@ extern "C" int gemm_f32_status(gemm_f32_stream_t stream_handle, unsigned* site) 
   }
   if (site) *site = word;
   return word ? GEMM_F32_ETIMEOUT : GEMM_F32_OK;
+}
+
+extern "C" int gemm_f32_clock_record(gemm_f32_stream_t stream_handle,
+                                     unsigned long long* sm_cycles, unsigned long long* ns) {
+  if (sm_cycles) *sm_cycles = 0;
+  if (ns) *ns = 0;
+  if (!sm_cycles || !ns) return GEMM_F32_EINVAL;
+  int dev = 0;
+  DeviceState* st = device_state(&dev);
+  if (!st || st->status != GEMM_F32_OK) return GEMM_F32_EDEVICE;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream_handle)) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
+  unsigned long long rec[2] = {0, 0};
+  if (cudaMemcpy(rec, st->err + 4, sizeof(rec), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return GEMM_F32_ELAUNCH;
+  }
+  *sm_cycles = rec[0];
+  *ns = rec[1];
+  return GEMM_F32_OK;
 }
 
 extern "C" int gemm_f32_release(void) {

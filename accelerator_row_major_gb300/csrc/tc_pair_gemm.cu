@@ -340,8 +340,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   volatile int* const pending_count =
       reinterpret_cast<volatile int*>(base_ptr + (tmem_slot + 8u - base));
   WorkItem* const pending = reinterpret_cast<WorkItem*>(base_ptr + (tmem_slot + 16u - base));
-  static_assert(8 * (4 * S + 3) + 16 + kMaxPending * sizeof(WorkItem) <= 1024,
+  static_assert(8 * (4 * S + 3) + 16 + kMaxPending * sizeof(WorkItem) <= 1024 - 16,
                 "barriers and pending work fit the 1024 bytes after the stages");
+  // the clock record's start mark: the last 16 bytes of that region
+  unsigned long long(&clk_mark)[2] =
+      *reinterpret_cast<unsigned long long(*)[2]>(base_ptr + (bars + 1008u - base));
+  clock_start(clk_mark);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -744,6 +748,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   }
+  clock_stop(p.err, clk_mark);
   if (p.sk_ctas > 0 && threadIdx.x == 0) tail_launch_done(p.counters);
 }
 

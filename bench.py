@@ -365,12 +365,25 @@ def run_reference(args):
 def roofline(kernel, mode, flop, work_bytes, t_kernel, rates, clocks, peaks, peak_src):
     """The binding roof of one launch of `kernel`.  Compute roofs are the
     probed per-SM rate of the unit doing the work (gemm_f32_unit_rates: FLOP
-    per SM per clock) x SMs x the median SM clock sampled while the steps ran;
-    the memory roof is the measured copy bandwidth."""
+    per SM per clock) x SMs x the SM clock the timed launches ran at: the
+    kernels' own clock record when the summary has it, else the median
+    nvidia-smi sample (under a tensor-core load the SMs run well below the
+    clock nvidia-smi reports, so the record is the one that bounds the
+    kernel; the roof at the reported clock is kept beside it).  The memory
+    roof is the measured copy bandwidth."""
     sms = rates["num_sms"]
-    mhz = clocks["sm_mhz"] if clocks else rates["sm_mhz"]
-    clock_src = "median SM clock sampled over the %s" % clocks["window"] if clocks else \
-        "SM clock during the unit probe (no nvidia-smi samples)"
+    smi_mhz = clocks.get("sm_mhz") if clocks else None
+    kernel_mhz = clocks.get("kernel_sm_mhz") if clocks else None
+    if kernel_mhz:
+        mhz = kernel_mhz
+        clock_src = "SM clock of the timed launches, measured in the kernels: clock64 / " \
+                    "%globaltimer of CTA 0"
+    elif smi_mhz:
+        mhz = smi_mhz
+        clock_src = "median SM clock sampled over the %s" % clocks["window"]
+    else:
+        mhz = rates["sm_mhz"]
+        clock_src = "SM clock during the unit probe (no clock samples)"
     if mode == "ffma":
         peak = rates["ffma_flop_per_clk_sm"] * sms * mhz * 1e6 / 1e12
         roof = {"bound": "alu", "achieved": flop / t_kernel / 1e12, "peak": peak, "unit": "TFLOP/s",
@@ -401,6 +414,10 @@ def roofline(kernel, mode, flop, work_bytes, t_kernel, rates, clocks, peaks, pea
                                                 "1.1/2.25" % peak_src}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["frac_of"] = "measured"
+    if roof["bound"] != "hbm" and kernel_mhz and smi_mhz:
+        # the same roof at the clock nvidia-smi reported for the window
+        at = roof["peak"] * smi_mhz / kernel_mhz
+        roof["at_reported_clock"] = {"sm_mhz": smi_mhz, "peak": at, "frac": roof["achieved"] / at}
     return roof
 
 
@@ -431,6 +448,7 @@ def time_product(g, A, B, C, M, N, K, mode, flags, stream, steps, warmup, flush,
             raise SystemExit("device error word %d after warm-up" % site)
         barrier(dist_mod, device)
         torch.cuda.synchronize(device)
+        rec0 = g.gemm_f32_clock_record(stream)
         t_start = time.time()
         with torch.cuda.stream(stream):
             if flush:
@@ -452,13 +470,29 @@ def time_product(g, A, B, C, M, N, K, mode, flags, stream, steps, warmup, flush,
                 events.append((e0, e1))
         torch.cuda.synchronize(device)
         t_end = time.time()
+        rec1 = g.gemm_f32_clock_record(stream)
         barrier(dist_mod, device)
     device_ms = sum(a.elapsed_time(b) for a, b in events)
     rc, site = g.gemm_f32_status(stream)
     if rc != 0:
         raise SystemExit("device error word %d in the timed region" % site)
     ms_per_step = max_over_ranks(device_ms / steps, dist_mod, device)
-    return ms_per_step, launches_per_step, kernel, clocks.summary(t_start, t_end)
+    return ms_per_step, launches_per_step, kernel, with_kernel_clock(clocks.summary(t_start, t_end),
+                                                                     rec0, rec1)
+
+
+def with_kernel_clock(summary, rec0, rec1):
+    """The clock summary with the SM clock the timed launches ran at, from
+    the kernels' own clock record (gemm_f32_clock_record read before and
+    after them): SM clocks / nanoseconds of CTA 0 over those launches."""
+    cycles, ns = rec1[0] - rec0[0], rec1[1] - rec0[1]
+    if ns <= 0 or cycles <= 0:
+        return summary
+    out = dict(summary) if summary else {}
+    out["kernel_sm_mhz"] = 1e3 * cycles / ns
+    out["kernel_clock"] = ("clock64 / %globaltimer of CTA 0 of each timed launch, summed "
+                           "(gemm_f32_clock_record)")
+    return out
 
 
 # modes reported beside the headline one, on the same problem, when the

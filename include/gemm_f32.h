@@ -140,6 +140,25 @@ int gemm_f32_ex(const float* A, const float* B, float* C, int M, int N, int K,
  * wait that gave up (0 if none). */
 int gemm_f32_status(gemm_f32_stream_t stream, unsigned* site);
 
+/* The clock record of the current device.  The first thread of CTA 0 of
+ * every tc_pair_kernel and ffma_gemm_kernel launch adds that CTA's lifetime
+ * to two running sums: SM clock cycles (clock64) and nanoseconds
+ * (%globaltimer).  tc_gemm_kernel and the small and teaching kernels add
+ * nothing.  The persistent grids keep CTA 0 for the
+ * whole launch, so the difference of two readings taken around a run of
+ * launches, cycles / ns, is the SM clock those launches ran at.  That is
+ * the clock a compute roofline needs ("Lesson 10: shared-memory tiled
+ * GEMM", hpc.payai.win, section 1: the peak is a rate per clock times the
+ * clock).  It can sit well below the clock the driver reports under a
+ * tensor-core load.  The call synchronises `stream` and copies the two sums
+ * to *sm_cycles and *ns, which must not be NULL.  The sums count from the
+ * library's set-up on the device.  Launches running on several streams at
+ * once add to the same sums.  Returns 0, GEMM_F32_EINVAL (a NULL output),
+ * GEMM_F32_EDEVICE or GEMM_F32_ELAUNCH (the synchronisation or the copy
+ * failed). */
+int gemm_f32_clock_record(gemm_f32_stream_t stream, unsigned long long* sm_cycles,
+                          unsigned long long* ns);
+
 /* Number of kernels the last successful call on this host thread launched
  * (0 for a no-op, 1 for a GEMM or for the K == 0 memset, plus one per launch
  * that copied operands for the tensor-memory accelerator). */

@@ -25,7 +25,7 @@ def test_header_declares_the_entry_points(g):
                             "gemm_f32_general", "gemm_f32_host",
                             "gemm_f32_last_kernel", "gemm_f32_last_launches", "gemm_f32_noalloc",
                             "gemm_f32_release", "gemm_f32_unit_rates",
-                            "gemm_f32_version"])
+                            "gemm_f32_clock_record", "gemm_f32_version"])
 
 
 def test_library_exports_every_declared_symbol(g):
@@ -48,6 +48,15 @@ def test_version(g):
 def test_unit_rates_rejects_a_null_record(g):
     from accelerator_row_major_gb300 import _binding
     assert _binding.lib().gemm_f32_unit_rates(None) == g.GEMM_F32_EINVAL
+
+
+def test_clock_record_rejects_null_outputs(g):
+    # checked before the device is touched, so this runs without a GPU
+    from accelerator_row_major_gb300 import _binding
+    c = ctypes.c_ulonglong(7)
+    assert _binding.lib().gemm_f32_clock_record(None, None, ctypes.byref(c)) == g.GEMM_F32_EINVAL
+    assert c.value == 0
+    assert _binding.lib().gemm_f32_clock_record(None, ctypes.byref(c), None) == g.GEMM_F32_EINVAL
 
 
 def test_tile224_flag_is_known_and_exclusive(g):

@@ -126,6 +126,27 @@ def test_roofline_takes_the_probed_rate_times_the_sampled_clock():
     assert abs(noclk["peak"] - 250.0 * 100 * 1500e6 / 1e12) < 1e-9
 
 
+def test_roofline_prefers_the_kernels_own_clock():
+    flop, nbytes = 2 * 8192 ** 3, 4 * 3 * 8192 ** 2
+    clocks = bench.with_kernel_clock({"sm_mhz": 2070.0, "window": "timed steps"},
+                                     (1000, 2000), (1000 + 1_750_000, 2000 + 1_000_000))
+    assert abs(clocks["kernel_sm_mhz"] - 1750.0) < 1e-9     # 1.75 M clocks in 1 ms
+    pair = bench.roofline("tc_pair_kernel", "tc3x", flop, nbytes, 1e-3, RATES, clocks, PEAKS, "measured")
+    assert abs(pair["peak"] - 4096.0 * 100 * 1750e6 / 1e12) < 1e-9
+    at = pair["at_reported_clock"]
+    assert at["sm_mhz"] == 2070.0 and abs(at["peak"] - 4096.0 * 100 * 2070e6 / 1e12) < 1e-9
+    assert abs(at["frac"] - pair["achieved"] / at["peak"]) < 1e-12 and at["frac"] < pair["frac"]
+    # a record that did not move (no persistent launch timed) leaves the summary as it was
+    same = {"sm_mhz": 2070.0, "window": "timed steps"}
+    assert bench.with_kernel_clock(same, (5, 5), (5, 5)) == same
+    assert bench.with_kernel_clock(None, (0, 0), (100, 50))["kernel_sm_mhz"] == 2000.0
+    # the memory roof does not depend on the clock
+    M, K, N = 65536, 1024, 64
+    r = bench.roofline("tc_gemm_kernel", "tc3x", 2 * M * N * K, 4 * (M * K + K * N + M * N), 60e-6,
+                       RATES, clocks, PEAKS, "measured")
+    assert r["bound"] == "hbm" and "at_reported_clock" not in r
+
+
 def test_roofline_of_a_skinny_shape_is_memory_bound():
     M, K, N = 65536, 1024, 64
     flop, nbytes = 2 * M * N * K, 4 * (M * K + K * N + M * N)
