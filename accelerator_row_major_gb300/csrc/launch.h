@@ -76,8 +76,9 @@ void* acquire_workspace(int device, cudaStream_t stream, size_t bytes);
 int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 
 // Tensor-core path on CTA pairs (256 x 256 tiles, cta_group::2), and whether
-// a problem should take it (large M and N, or forced by flags).
-bool tc_pair_suits(const GemmArgs& g);
+// a problem in a mode of `nprod` products should take it (a wave of pair
+// tiles and, on the TMA path, a deep enough K; or forced by flags).
+bool tc_pair_suits(const GemmArgs& g, int nprod);
 int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches);
 
 // Tensor-core path on the single-CTA kernel whose split-tail scratch is the

@@ -1066,20 +1066,11 @@ int launch_tc(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
 }
 
 int launch_tc_kernels(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {
-  if (tc_pair_suits(g)) return launch_tc_pair(g, nprod, stream, launches);
-  // One product does a third of the MMA work per stage, which leaves the
-  // single-CTA kernel's shared-memory traffic exposed; the pair kernel halves
-  // it and pays off at fewer tiles (measured on GB300: 2048^3 34.0 against
-  // 44.0 us, 2048 x 1024 x 4096 40.7 against 50.8 us), unless shorter tiles
-  // fill one wave (1536^3: 24.2 us single against 26.7 us pair).  Only on
-  // the TMA path: with per-thread loads the single-CTA kernel is faster
-  // (1001 x 513 x 777: 31.6 against 55 us).
-  const unsigned no_pair = GEMM_F32_FLAG_SINGLE_CTA | GEMM_F32_FLAG_TILE64 |
-                           GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE224 | GEMM_F32_FLAG_TILE256 |
-                           GEMM_F32_FLAG_ONE_TILE_PER_CTA | GEMM_F32_FLAG_FORCE_STAGED;
-  if (nprod == 1 && !(g.flags & no_pair) && tma_addressable(g) && g.M >= 256 && g.N >= 256 &&
-      !one_wave_height(g, kTN))
-    return launch_tc_pair(g, nprod, stream, launches);
+  // Below a wave of pair tiles the single-SM kernel is faster in both modes
+  // (measured on GB300, one product, CUDA-graph replay: 2048^3 25.2 against
+  // 28.8 us; M = 1001, K = 777, N = 513 15.9 against 21.7 us; M = N = 1024,
+  // K = 8192 42.1 against 46.6 us).
+  if (tc_pair_suits(g, nprod)) return launch_tc_pair(g, nprod, stream, launches);
   return launch_tc_single(g, nprod, TailScratch(), stream, launches);
 }
 

@@ -780,7 +780,19 @@ int launch_pair_one(const GemmArgs& g, const PairParams& p, const PairGeneral& g
 
 }  // namespace
 
-bool tc_pair_suits(const GemmArgs& g) {
+// Least K for the pair kernel on the TMA path, with three products and with
+// one.  Its single accumulator makes each tile's MMAs wait for the previous
+// tile's epilogue (about 7,000 clocks), against a tile's MMA work of 48 K
+// clocks (three products) or 16 K (one).  Measured on GB300 (CUDA-graph
+// replay, against single-SM tiles): three products, 4096^3 391.6 against
+// 399.5 us and 8192^3 3191 against 3346 us, but 4096 x 1024 x 4096 123.3
+// against 115.1 us and a tie at K = 2048 - 3072; one product, 8192^3 1499
+// against 1535 us, but 4096^3 206.3 against 198.7 us and 4096 x 1024 x 4096
+// 64.9 against 51.2 us.
+constexpr int kPairMinK3 = 3072;
+constexpr int kPairMinK1 = 6144;
+
+bool tc_pair_suits(const GemmArgs& g, int nprod) {
   if (g.flags & GEMM_F32_FLAG_SINGLE_CTA) return false;
   if (g.flags & GEMM_F32_FLAG_CTA_PAIR) return true;
   if (g.flags & (GEMM_F32_FLAG_TILE64 | GEMM_F32_FLAG_TILE128 | GEMM_F32_FLAG_TILE224 |
@@ -788,7 +800,10 @@ bool tc_pair_suits(const GemmArgs& g) {
     return false;
   const long tiles = static_cast<long>((g.M + kPairTile - 1) / kPairTile) *
                      ((g.N + kPairTile - 1) / kPairTile);
-  return g.M >= kPairTile && g.N >= kPairTile && tiles >= g.num_sms / 2;
+  if (g.M < kPairTile || g.N < kPairTile || tiles < g.num_sms / 2) return false;
+  if (!(g.flags & GEMM_F32_FLAG_FORCE_STAGED) && tma_addressable(g))
+    return g.K >= (nprod == 1 ? kPairMinK1 : kPairMinK3);
+  return true;   // per-thread loads: the pair kernel halves each SM's share
 }
 
 int launch_tc_pair(GemmArgs& g, int nprod, cudaStream_t stream, int* launches) {

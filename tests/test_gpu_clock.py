@@ -6,14 +6,16 @@ from tests._gpu import lib
 
 pytestmark = pytest.mark.gpu
 
-# (M, K, N), mode, the kernel that the library picks for it
-CASES = [((4096, 1024, 4096), "tc3x", "tc_pair_kernel"),
-         ((4096, 1024, 4096), "tc1x", "tc_pair_kernel"),
-         ((2048, 1024, 2048), "ffma", "ffma_gemm_kernel")]
+FLAG_CTA_PAIR = 0x400
+
+# (M, K, N), mode, flags, the kernel that runs
+CASES = [((4096, 1024, 4096), "tc3x", FLAG_CTA_PAIR, "tc_pair_kernel"),
+         ((4096, 1024, 4096), "tc1x", FLAG_CTA_PAIR, "tc_pair_kernel"),
+         ((2048, 1024, 2048), "ffma", 0, "ffma_gemm_kernel")]
 
 
-@pytest.mark.parametrize("shape,mode,kernel", CASES, ids=[c[2] for c in CASES])
-def test_clock_record_gives_the_sm_clock(shape, mode, kernel):
+@pytest.mark.parametrize("shape,mode,flags,kernel", CASES, ids=["%s-%s" % (c[3], c[1]) for c in CASES])
+def test_clock_record_gives_the_sm_clock(shape, mode, flags, kernel):
     import torch
 
     g = lib()
@@ -23,11 +25,11 @@ def test_clock_record_gives_the_sm_clock(shape, mode, kernel):
     B = torch.randn(K, N, device=dev)
     C = torch.empty(M, N, device=dev)
     stream = torch.cuda.current_stream()
-    g.check(g.gemm_f32_ex(A, B, C, M, N, K, mode, 0, stream))
+    g.check(g.gemm_f32_ex(A, B, C, M, N, K, mode, flags, stream))
     assert g.gemm_f32_last_kernel() == kernel
     c0, n0 = g.gemm_f32_clock_record(stream)
     for _ in range(5):
-        g.check(g.gemm_f32_ex(A, B, C, M, N, K, mode, 0, stream))
+        g.check(g.gemm_f32_ex(A, B, C, M, N, K, mode, flags, stream))
     c1, n1 = g.gemm_f32_clock_record(stream)
     assert c1 > c0 and n1 > n0
     ghz = (c1 - c0) / (n1 - n0)

@@ -57,7 +57,9 @@ def test_general_aligned_strides_take_the_tma_path(mode):
 @pytest.mark.parametrize("mode", ["tc3x", "tc1x"])
 @pytest.mark.parametrize("ta,tb,pads", [(0, 0, (4, 4, 4)), (1, 1, (3, 1, 2))])
 def test_general_on_the_pair_kernel(mode, ta, tb, pads):
-    M, N, K = 2304, 2560, 192
+    # 90 tiles of 256 x 256 and a K deep enough for the pair kernel on the
+    # TMA path (the operands are copied to TMA-readable form first)
+    M, N, K = 2304, 2560, (3072 if mode == "tc3x" else 6144)
     A, B, C0 = case(30 + ta, M, N, K, ta, tb, pads=pads)
     Co, absC = oracle.gemm_general(A, B, C0, M, N, K, alpha=0.75, beta=1.25, trans_a=ta, trans_b=tb)
     C = run_general(A, B, C0, M, N, K, 0.75, 1.25, ta, tb, mode)

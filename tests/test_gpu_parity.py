@@ -257,14 +257,21 @@ def test_last_kernel_names_the_path():
     g = lib()
     dev = torch.device("cuda:0")
     # 4096 x 4096 gives 256 tiles of 256 x 256: the pair path by default
-    A = torch.zeros((4096, 64), device=dev)
-    B = torch.zeros((64, 4096), device=dev)
+    # once K is deep enough (3072 with three products, 6144 with one), the
+    # single-SM path below that
+    A = torch.zeros((4096, 6144), device=dev)
+    B = torch.zeros((6144, 4096), device=dev)
     C = torch.empty((4096, 4096), device=dev)
     s = torch.cuda.current_stream(dev)
-    for mode, flags, want in (("tc3x", 0, "tc_pair_kernel"), ("tc3x", FLAG_SINGLE, "tc_gemm_kernel"),
-                              ("tc1x", 0, "tc_pair_kernel"), ("ffma", 0, "ffma_gemm_kernel")):
-        assert g.gemm_f32_ex(A, B, C, 4096, 4096, 64, mode, flags, s) == 0
-        assert g.gemm_f32_last_kernel() == want, (mode, flags)
+    for mode, K, flags, want in (("tc3x", 4096, 0, "tc_pair_kernel"),
+                                 ("tc3x", 4096, FLAG_SINGLE, "tc_gemm_kernel"),
+                                 ("tc3x", 1024, 0, "tc_gemm_kernel"),
+                                 ("tc3x", 1024, FLAG_PAIR, "tc_pair_kernel"),
+                                 ("tc1x", 6144, 0, "tc_pair_kernel"),
+                                 ("tc1x", 4096, 0, "tc_gemm_kernel"),
+                                 ("ffma", 64, 0, "ffma_gemm_kernel")):
+        assert g.gemm_f32_ex(A, B, C, 4096, 4096, K, mode, flags, s) == 0
+        assert g.gemm_f32_last_kernel() == want, (mode, K, flags)
     assert g.gemm_f32_ex(A, B, C, 4096, 4096, 0, "tc3x", 0, s) == 0
     assert g.gemm_f32_last_kernel() == "memset"
     # small products take the small CUDA-core kernel in every mode, unless a
