@@ -99,7 +99,10 @@ enum gemm_f32_mode {
 #define GEMM_F32_FLAG_CTA_PAIR 0x400u    /* tensor modes: compute 256 x 256
                                             tiles on pairs of SMs (cluster of
                                             two CTAs, one M = 256 MMA); the
-                                            default for large M and N         */
+                                            default with a wave of such tiles
+                                            and a deep K (on TMA-readable
+                                            operands K >= 3072 in tc3x, K >=
+                                            6144 in tc1x)                     */
 #define GEMM_F32_FLAG_SINGLE_CTA 0x800u  /* tensor modes: one CTA per tile    */
 #define GEMM_F32_FLAG_TEST_DROP_COPY 0x1000u /* testing only, on the TMA
                                             path of every mode: CTA 0 never
