@@ -267,7 +267,10 @@ def test_last_kernel_names_the_path():
                                  ("tc3x", 4096, FLAG_SINGLE, "tc_gemm_kernel"),
                                  ("tc3x", 1024, 0, "tc_gemm_kernel"),
                                  ("tc3x", 1024, FLAG_PAIR, "tc_pair_kernel"),
+                                 ("tc3x", 3068, 0, "tc_gemm_kernel"),    # just below the K bound
+                                 ("tc3x", 3072, 0, "tc_pair_kernel"),    # at it
                                  ("tc1x", 6144, 0, "tc_pair_kernel"),
+                                 ("tc1x", 6140, 0, "tc_gemm_kernel"),
                                  ("tc1x", 4096, 0, "tc_gemm_kernel"),
                                  ("ffma", 64, 0, "ffma_gemm_kernel")):
         assert g.gemm_f32_ex(A, B, C, 4096, 4096, K, mode, flags, s) == 0
